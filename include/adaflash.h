@@ -1,0 +1,166 @@
+/*
+ * adaflash.h -- C ABI of the packed verify + on-policy-distillation (OPD) loss pass.
+ *
+ * The operations come from the page "AdaFlash: Adaptive Speculative Decoding with
+ * Online Self-Improvement for High-Concurrency LLM Inference" (below: the AdaFlash
+ * article) and the page "AdaFlash: Adaptive Speculative Decoding via On-Policy
+ * Distilled Diffusion Drafters" (below: the AdaFlash README).
+ *
+ * Packed layout ("Variable-length request packing", AdaFlash article): R requests
+ * with draft lengths 1 <= k_i <= 16 share one batch.  draft_offsets (int32, R+1
+ * entries) is the exclusive prefix sum of the k_i, so draft_offsets[0] = 0 and
+ * draft_offsets[R] = N_d, the number of draft rows.  Request i owns
+ *   - draft rows   draft_offsets[i] .. draft_offsets[i+1]-1      (k_i rows),
+ *   - target rows  draft_offsets[i]+i .. draft_offsets[i+1]+i    (k_i+1 rows),
+ * so there are N_t = N_d + R target rows.  Draft row draft_offsets[i]+j is paired
+ * with target row draft_offsets[i]+i+j (the target's distribution at the position
+ * of draft token j); target row draft_offsets[i+1]+i is the request's bonus row.
+ *
+ * Logit matrices are row-major: row r of a matrix with leading dimension ld starts
+ * at element r*ld; columns ld > vocab are never read.  Element types: float32 or
+ * bfloat16 (ADAFLASH_FP32 / ADAFLASH_BF16); supported (draft, target) pairs are
+ * (fp32, fp32), (bf16, bf16), (fp32, bf16) and (bf16, fp32).  Any element-aligned
+ * base pointer and any ld >= vocab are accepted; rows whose start is 16-byte
+ * aligned take the bulk-copy path, others a slower direct-load path.
+ *
+ * Ownership and ordering: every pointer argument is a DEVICE pointer owned by the
+ * caller.  The library allocates nothing, keeps no state between calls and never
+ * synchronises: each call enqueues its kernels on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and returns.  Calls on one stream run in order.
+ *
+ * Errors:
+ *   - Argument errors found on the host are returned at once and nothing is
+ *     enqueued (ADAFLASH_ERR_INVALID_ARG, ADAFLASH_ERR_UNSUPPORTED).
+ *   - A failed CUDA launch returns ADAFLASH_ERR_CUDA.
+ *   - Errors only the device can see are OR-ed into *d_status as bit
+ *     (1u << code), e.g. (1u << ADAFLASH_ERR_BAD_OFFSETS); d_status may be NULL
+ *     to ignore them.  The library never clears *d_status.  A row or request
+ *     with such an error is skipped (its outputs are left unwritten, or set to
+ *     -1 where stated); the kernels never trap or fault on bad device data.
+ *
+ * Device: compute capability 10.3 (GB300, sm_103a).  Any other device gives
+ * ADAFLASH_ERR_UNSUPPORTED.
+ */
+#ifndef ADAFLASH_H
+#define ADAFLASH_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ADAFLASH_OK = 0,
+  ADAFLASH_ERR_INVALID_ARG = 1, /* host: NULL pointer, vocab < 1, ld < vocab, bad dtype, bad counts, clip_c not > 0 */
+  ADAFLASH_ERR_UNSUPPORTED = 2, /* host: device is not cc 10.3, or vocab above the supported maximum */
+  ADAFLASH_ERR_CUDA = 3,        /* host: a CUDA runtime call or launch failed */
+  ADAFLASH_ERR_TIMEOUT = 4,     /* device bit: a bounded wait gave up; that row's outputs are invalid */
+  ADAFLASH_ERR_BAD_OFFSETS = 5, /* device bit: draft_offsets not a prefix sum of k_i in [1,16] ending at N_d */
+  ADAFLASH_ERR_BAD_TOKEN = 6    /* device bit: a draft token outside [0, vocab); it never counts as accepted */
+} adaflash_status;
+
+typedef enum { ADAFLASH_FP32 = 0, ADAFLASH_BF16 = 1 } adaflash_dtype;
+
+/* Largest vocabulary the kernels accept (8 CTAs x 65536 entries per row). */
+#define ADAFLASH_MAX_VOCAB 524288
+/* Largest draft length of one request (the fixed verification length k = 16 of
+ * the AdaFlash article, section "2. Adaptive Length Head for Token-Level Variance"). */
+#define ADAFLASH_MAX_K 16
+
+/*
+ * adaflash_verify_packed -- greedy verification of packed draft blocks.
+ *
+ * The draft model proposes k_i tokens and the target verifies them in parallel
+ * (AdaFlash article, opening section); the true acceptance rate is the length
+ * head's free label (section "2. Adaptive Length Head for Token-Level Variance").
+ * Greedy reading: the target's choice at a position is the lowest index of the
+ * row maximum; draft token j is accepted while it equals that choice.
+ *
+ *   target_logits  [N_t, ld_t] of t_dtype          in
+ *   draft_tokens   int32 [N_d]                      in
+ *   draft_offsets  int32 [R+1]                      in
+ *   target_argmax  int32 [N_t]                      out: lowest index of each target row's maximum
+ *   accept_len     int32 [R]                        out: L_i = first j with token != choice, else k_i
+ *   bonus_token    int32 [R]                        out: target choice at target row draft_offsets[i]+i+L_i
+ *   accept_rate    float [R]                        out: L_i / k_i rounded once to float32
+ * A request with malformed offsets gets accept_len = bonus_token = -1.
+ */
+adaflash_status adaflash_verify_packed(
+    const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
+    const int32_t* draft_tokens, const int32_t* draft_offsets,
+    int32_t num_requests, int32_t num_draft_rows, int32_t vocab,
+    int32_t* target_argmax, int32_t* accept_len, int32_t* bonus_token, float* accept_rate,
+    uint32_t* d_status, void* stream);
+
+/*
+ * adaflash_opd_loss_fwd -- fused verification + OPD loss forward (one read of every logit).
+ *
+ * For each draft row d (request i, position j) with draft logits z and paired
+ * target logits t, p = softmax(z), q = softmax(t), r_v = log p_v - log q_v:
+ *   kl_row[d] = sum_v min(p_v r_v, clip_c)  -- the reverse KL(p||q) with each
+ *               vocabulary term clipped before the sum (AdaFlash article,
+ *               "Reverse KL + Top-1 hard labels" and "Per-vocabulary divergence
+ *               clipping"; the clip bounds terms from above);
+ *   ce_row[d] = -log p_a, a = target_argmax of the paired target row
+ *               ("Top-1 hard labels from the target");
+ *   loss[0]   = (1/N_d) sum_d (kl_row[d] + ce_weight * ce_row[d])  (the
+ *               "mixture reverse-KL loss" of the AdaFlash README, "Released Checkpoint").
+ * It also produces every output of adaflash_verify_packed, and
+ *   row_stats [N_d, 4] float: {logsumexp(z), logsumexp(t), S, n_clipped} with
+ *               S = sum_v [p_v r_v <= clip_c] p_v (r_v + 1); pass it to the backward.
+ * clip_c must be > 0 (+inf disables the clip); ce_weight is the mixture weight.
+ */
+adaflash_status adaflash_opd_loss_fwd(
+    const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
+    const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
+    const int32_t* draft_tokens, const int32_t* draft_offsets,
+    int32_t num_requests, int32_t num_draft_rows, int32_t vocab,
+    float clip_c, float ce_weight,
+    int32_t* target_argmax, int32_t* accept_len, int32_t* bonus_token, float* accept_rate,
+    float* kl_row, float* ce_row, float* row_stats, float* loss,
+    uint32_t* d_status, void* stream);
+
+/*
+ * adaflash_opd_loss_bwd -- gradient of the OPD loss with respect to the draft logits.
+ *
+ * Training updates the serving draft model from each round's verification
+ * (AdaFlash article, "On-Policy Distillation (OPD) for Domain Adaptation"); the
+ * target is a constant ("the target model never changes").  With g_r =
+ * grad_row[r] (or grad_scale when grad_row is NULL), m_v = [p_v r_v <= clip_c]
+ * and a the target argmax:
+ *   grad_draft[r, v] = g_r * ( p_v (m_v (r_v + 1) - S) + ce_weight (p_v - [v == a]) )
+ * where S and the two log-sum-exps come from row_stats of the forward and a from
+ * its target_argmax.  grad_draft is float32 [N_d, ld_g]; columns >= vocab are not
+ * written.  grad_scale = 1/N_d gives the gradient of the mean loss.
+ */
+adaflash_status adaflash_opd_loss_bwd(
+    const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
+    const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
+    const int32_t* draft_offsets, int32_t num_requests, int32_t num_draft_rows, int32_t vocab,
+    float clip_c, float ce_weight,
+    const int32_t* target_argmax, const float* row_stats,
+    const float* grad_row, float grad_scale,
+    float* grad_draft, int64_t ld_g,
+    uint32_t* d_status, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* adaflash_status_string(adaflash_status status);
+
+/*
+ * adaflash_selftest_bounded_wait -- exercises the bounded-wait error path.
+ *
+ * Launches one block that waits on a shared-memory barrier nothing ever
+ * completes, with a limit of `limit_us` microseconds (1 .. 1000000); the wait
+ * gives up, the block sets bit (1u << ADAFLASH_ERR_TIMEOUT) in *d_status and
+ * returns.  This is the same wait routine the streaming kernels use, so a test
+ * can check on a real device that a stuck wait ends in a status, not a hang.
+ * The pages have no counterpart: it is part of this library's failure handling.
+ */
+adaflash_status adaflash_selftest_bounded_wait(uint32_t* d_status, int32_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADAFLASH_H */

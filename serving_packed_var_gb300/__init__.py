@@ -1,0 +1,167 @@
+"""Packed verify + on-policy-distillation loss pass for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libadaflash.so`` (include/adaflash.h).
+The functions keep the C names and only marshal arguments: torch tensors are
+turned into device pointers, strides and the current stream; missing outputs are
+allocated with torch.  Every step of the computation runs in the CUDA kernels.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import _native
+from ._native import (  # noqa: F401
+    ADAFLASH_BF16,
+    ADAFLASH_ERR_BAD_OFFSETS,
+    ADAFLASH_ERR_BAD_TOKEN,
+    ADAFLASH_ERR_CUDA,
+    ADAFLASH_ERR_INVALID_ARG,
+    ADAFLASH_ERR_TIMEOUT,
+    ADAFLASH_ERR_UNSUPPORTED,
+    ADAFLASH_FP32,
+    ADAFLASH_MAX_VOCAB,
+    ADAFLASH_OK,
+    LibraryMissing,
+)
+
+__all__ = [
+    "AdaflashError",
+    "adaflash_verify_packed",
+    "adaflash_opd_loss_fwd",
+    "adaflash_opd_loss_bwd",
+    "adaflash_selftest_bounded_wait",
+    "adaflash_status_string",
+    "status_bits",
+]
+
+
+class AdaflashError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {_native.status_string(code)} ({code})")
+
+
+def adaflash_status_string(code: int) -> str:
+    return _native.status_string(code)
+
+
+def status_bits(word: int):
+    """Status codes set in a device status word."""
+    return [c for c in range(1, 7) if word & (1 << c)]
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return ADAFLASH_FP32
+    if t.dtype == torch.bfloat16:
+        return ADAFLASH_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _rows(t: torch.Tensor, name: str):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D row-major view (stride(1) == 1)")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.data_ptr(), t.stride(0)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(code: int, where: str):
+    if code != ADAFLASH_OK:
+        raise AdaflashError(code, where)
+
+
+def _i32(n, dev):
+    return torch.empty(n, dtype=torch.int32, device=dev)
+
+
+def _f32(n, dev):
+    return torch.empty(n, dtype=torch.float32, device=dev)
+
+
+def adaflash_verify_packed(target_logits, draft_tokens, draft_offsets, vocab=None, out=None, status=None,
+                           stream=None):
+    """Greedy verification.  Returns dict(target_argmax, accept_len, bonus_token, accept_rate)."""
+    tp, ldt = _rows(target_logits, "target_logits")
+    dev = target_logits.device
+    R = draft_offsets.numel() - 1
+    Nd = draft_tokens.numel()
+    V = target_logits.shape[1] if vocab is None else vocab
+    o = dict(out or {})
+    o.setdefault("target_argmax", _i32(Nd + R, dev))
+    o.setdefault("accept_len", _i32(R, dev))
+    o.setdefault("bonus_token", _i32(R, dev))
+    o.setdefault("accept_rate", _f32(R, dev))
+    code = _native.lib().adaflash_verify_packed(
+        tp, _dtype_code(target_logits), ldt, draft_tokens.data_ptr(), draft_offsets.data_ptr(), R, Nd, V,
+        o["target_argmax"].data_ptr(), o["accept_len"].data_ptr(), o["bonus_token"].data_ptr(),
+        o["accept_rate"].data_ptr(), _ptr(status), _stream(stream))
+    _check(code, "adaflash_verify_packed")
+    return o
+
+
+def adaflash_opd_loss_fwd(draft_logits, target_logits, draft_tokens, draft_offsets, clip_c, ce_weight=1.0,
+                          vocab=None, out=None, status=None, stream=None):
+    """Fused verification + OPD loss forward.
+
+    Returns dict(target_argmax, accept_len, bonus_token, accept_rate, kl_row, ce_row, row_stats, loss).
+    """
+    zp, ldz = _rows(draft_logits, "draft_logits")
+    tp, ldt = _rows(target_logits, "target_logits")
+    dev = draft_logits.device
+    R = draft_offsets.numel() - 1
+    Nd = draft_tokens.numel()
+    V = draft_logits.shape[1] if vocab is None else vocab
+    o = dict(out or {})
+    o.setdefault("target_argmax", _i32(Nd + R, dev))
+    o.setdefault("accept_len", _i32(R, dev))
+    o.setdefault("bonus_token", _i32(R, dev))
+    o.setdefault("accept_rate", _f32(R, dev))
+    o.setdefault("kl_row", _f32(Nd, dev))
+    o.setdefault("ce_row", _f32(Nd, dev))
+    o.setdefault("row_stats", torch.empty((Nd, 4), dtype=torch.float32, device=dev))
+    o.setdefault("loss", _f32(1, dev))
+    code = _native.lib().adaflash_opd_loss_fwd(
+        zp, _dtype_code(draft_logits), ldz, tp, _dtype_code(target_logits), ldt,
+        draft_tokens.data_ptr(), draft_offsets.data_ptr(), R, Nd, V, float(clip_c), float(ce_weight),
+        o["target_argmax"].data_ptr(), o["accept_len"].data_ptr(), o["bonus_token"].data_ptr(),
+        o["accept_rate"].data_ptr(), o["kl_row"].data_ptr(), o["ce_row"].data_ptr(), o["row_stats"].data_ptr(),
+        o["loss"].data_ptr(), _ptr(status), _stream(stream))
+    _check(code, "adaflash_opd_loss_fwd")
+    return o
+
+
+def adaflash_opd_loss_bwd(draft_logits, target_logits, draft_offsets, target_argmax, row_stats, clip_c,
+                          ce_weight=1.0, grad_row=None, grad_scale=1.0, vocab=None, out=None, status=None,
+                          stream=None):
+    """Gradient of sum_r g_r * loss_row with respect to the draft logits (float32)."""
+    zp, ldz = _rows(draft_logits, "draft_logits")
+    tp, ldt = _rows(target_logits, "target_logits")
+    R = draft_offsets.numel() - 1
+    Nd = draft_logits.shape[0]
+    V = draft_logits.shape[1] if vocab is None else vocab
+    g = out if out is not None else torch.empty((Nd, V), dtype=torch.float32, device=draft_logits.device)
+    gp, ldg = _rows(g, "grad_draft")
+    if g.dtype != torch.float32:
+        raise TypeError("grad_draft must be float32")
+    code = _native.lib().adaflash_opd_loss_bwd(
+        zp, _dtype_code(draft_logits), ldz, tp, _dtype_code(target_logits), ldt, draft_offsets.data_ptr(),
+        R, Nd, V, float(clip_c), float(ce_weight), target_argmax.data_ptr(), row_stats.data_ptr(),
+        _ptr(grad_row), float(grad_scale), gp, ldg, _ptr(status), _stream(stream))
+    _check(code, "adaflash_opd_loss_bwd")
+    return g
+
+
+def adaflash_selftest_bounded_wait(status, limit_us=1000, stream=None):
+    code = _native.lib().adaflash_selftest_bounded_wait(status.data_ptr(), int(limit_us), _stream(stream))
+    _check(code, "adaflash_selftest_bounded_wait")

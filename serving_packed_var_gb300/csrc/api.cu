@@ -1,0 +1,254 @@
+// api.cu -- the extern "C" entry points declared in include/adaflash.h.
+//
+// Host-side argument validation happens before any CUDA call, so malformed calls
+// return at once and enqueue nothing.  Every accepted call enqueues its kernels on
+// the caller's stream and returns without synchronising.
+#include <cmath>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/adaflash.h"
+#include "kernels.h"
+
+using namespace adaflash;
+
+namespace {
+
+bool valid_dtype(adaflash_dtype t) { return t == ADAFLASH_FP32 || t == ADAFLASH_BF16; }
+int dtype_bytes(adaflash_dtype t) { return t == ADAFLASH_FP32 ? 4 : 2; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Rows of a [N, ld] matrix start on 16-byte boundaries (bulk-copy / 128-bit path).
+bool rows_16b(const void* base, int64_t ld, int bytes) {
+  return aligned(base, 16) && ((ld * bytes) % 16 == 0);
+}
+
+// Shape checks shared by all entry points.
+adaflash_status check_shape(int32_t R, int32_t N_d, int32_t V) {
+  if (V < 1 || R < 0 || N_d < 0) return ADAFLASH_ERR_INVALID_ARG;
+  if (V > ADAFLASH_MAX_VOCAB) return ADAFLASH_ERR_UNSUPPORTED;
+  if (R == 0 && N_d != 0) return ADAFLASH_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(N_d) < R || static_cast<int64_t>(N_d) > static_cast<int64_t>(ADAFLASH_MAX_K) * R)
+    return ADAFLASH_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(N_d) + R > INT32_MAX) return ADAFLASH_ERR_INVALID_ARG;
+  return ADAFLASH_OK;
+}
+
+adaflash_status check_logits(const void* p, adaflash_dtype dt, int64_t ld, int32_t V) {
+  if (!p || !valid_dtype(dt) || ld < V) return ADAFLASH_ERR_INVALID_ARG;
+  if (!aligned(p, static_cast<uintptr_t>(dtype_bytes(dt)))) return ADAFLASH_ERR_INVALID_ARG;
+  return ADAFLASH_OK;
+}
+
+bool int_ptr_ok(const void* p) { return p && aligned(p, 4); }
+
+// The device must be compute capability 10.3 (checked once per device).
+adaflash_status check_device() {
+  static int cache[64];  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ADAFLASH_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev] == 1 ? ADAFLASH_OK : ADAFLASH_ERR_UNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return ADAFLASH_ERR_CUDA;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+  return ok ? ADAFLASH_OK : ADAFLASH_ERR_UNSUPPORTED;
+}
+
+#define ADAFLASH_TRY(expr)                          \
+  do {                                              \
+    const adaflash_status st_ = (expr);             \
+    if (st_ != ADAFLASH_OK) return st_;             \
+  } while (0)
+
+#define ADAFLASH_CUDA(expr)                              \
+  do {                                                   \
+    if ((expr) != cudaSuccess) return ADAFLASH_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* adaflash_status_string(adaflash_status s) {
+  switch (s) {
+    case ADAFLASH_OK: return "ADAFLASH_OK";
+    case ADAFLASH_ERR_INVALID_ARG: return "ADAFLASH_ERR_INVALID_ARG";
+    case ADAFLASH_ERR_UNSUPPORTED: return "ADAFLASH_ERR_UNSUPPORTED";
+    case ADAFLASH_ERR_CUDA: return "ADAFLASH_ERR_CUDA";
+    case ADAFLASH_ERR_TIMEOUT: return "ADAFLASH_ERR_TIMEOUT";
+    case ADAFLASH_ERR_BAD_OFFSETS: return "ADAFLASH_ERR_BAD_OFFSETS";
+    case ADAFLASH_ERR_BAD_TOKEN: return "ADAFLASH_ERR_BAD_TOKEN";
+  }
+  return "ADAFLASH_UNKNOWN_STATUS";
+}
+
+adaflash_status adaflash_verify_packed(const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
+                                       const int32_t* draft_tokens, const int32_t* draft_offsets,
+                                       int32_t num_requests, int32_t num_draft_rows, int32_t vocab,
+                                       int32_t* target_argmax, int32_t* accept_len, int32_t* bonus_token,
+                                       float* accept_rate, uint32_t* d_status, void* stream) {
+  ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  ADAFLASH_TRY(check_logits(target_logits, t_dtype, ld_t, vocab));
+  if (!int_ptr_ok(draft_tokens) || !int_ptr_ok(draft_offsets) || !int_ptr_ok(target_argmax) ||
+      !int_ptr_ok(accept_len) || !int_ptr_ok(bonus_token) || !int_ptr_ok(accept_rate))
+    return ADAFLASH_ERR_INVALID_ARG;
+  if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_device());
+  if (num_requests == 0) return ADAFLASH_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  RowPassParams p = {};
+  p.t = target_logits;
+  p.ld_t = ld_t;
+  p.doff = draft_offsets;
+  p.R = num_requests;
+  p.N_d = num_draft_rows;
+  p.N_t = num_draft_rows + num_requests;
+  p.V = vocab;
+  p.mode = kModeVerify;
+  p.cluster = rowpass_cluster_size(vocab);
+  p.slice = rowpass_slice(vocab, p.cluster);
+  p.clip_c = 1.0f;
+  p.target_argmax = target_argmax;
+  p.status = d_status;
+  // Target-only units read no draft row; the draft dtype only sizes the ring.
+  ADAFLASH_CUDA(launch_rowpass(p, 1, t_dtype, rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)), s));
+
+  FinalizeParams f = {};
+  f.tokens = draft_tokens;
+  f.doff = draft_offsets;
+  f.target_argmax = target_argmax;
+  f.R = num_requests;
+  f.N_d = num_draft_rows;
+  f.V = vocab;
+  f.accept_len = accept_len;
+  f.bonus_token = bonus_token;
+  f.accept_rate = accept_rate;
+  f.status = d_status;
+  ADAFLASH_CUDA(launch_finalize(f, s));
+  return ADAFLASH_OK;
+}
+
+adaflash_status adaflash_opd_loss_fwd(const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
+                                      const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
+                                      const int32_t* draft_tokens, const int32_t* draft_offsets,
+                                      int32_t num_requests, int32_t num_draft_rows, int32_t vocab, float clip_c,
+                                      float ce_weight, int32_t* target_argmax, int32_t* accept_len,
+                                      int32_t* bonus_token, float* accept_rate, float* kl_row, float* ce_row,
+                                      float* row_stats, float* loss, uint32_t* d_status, void* stream) {
+  ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  ADAFLASH_TRY(check_logits(draft_logits, d_dtype, ld_d, vocab));
+  ADAFLASH_TRY(check_logits(target_logits, t_dtype, ld_t, vocab));
+  if (!int_ptr_ok(draft_tokens) || !int_ptr_ok(draft_offsets) || !int_ptr_ok(target_argmax) ||
+      !int_ptr_ok(accept_len) || !int_ptr_ok(bonus_token) || !int_ptr_ok(accept_rate) || !int_ptr_ok(kl_row) ||
+      !int_ptr_ok(ce_row) || !int_ptr_ok(row_stats) || !int_ptr_ok(loss))
+    return ADAFLASH_ERR_INVALID_ARG;
+  if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
+  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight)) return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_device());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_requests == 0) {
+    ADAFLASH_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
+    return ADAFLASH_OK;
+  }
+
+  RowPassParams p = {};
+  p.z = draft_logits;
+  p.t = target_logits;
+  p.ld_z = ld_d;
+  p.ld_t = ld_t;
+  p.doff = draft_offsets;
+  p.R = num_requests;
+  p.N_d = num_draft_rows;
+  p.N_t = num_draft_rows + num_requests;
+  p.V = vocab;
+  p.mode = kModeFwd;
+  p.cluster = rowpass_cluster_size(vocab);
+  p.slice = rowpass_slice(vocab, p.cluster);
+  p.clip_c = clip_c;
+  p.target_argmax = target_argmax;
+  p.kl_row = kl_row;
+  p.ce_row = ce_row;
+  p.row_stats = row_stats;
+  p.status = d_status;
+  const bool fast = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
+                    rows_16b(target_logits, ld_t, dtype_bytes(t_dtype));
+  ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype, fast, s));
+
+  FinalizeParams f = {};
+  f.tokens = draft_tokens;
+  f.doff = draft_offsets;
+  f.target_argmax = target_argmax;
+  f.R = num_requests;
+  f.N_d = num_draft_rows;
+  f.V = vocab;
+  f.accept_len = accept_len;
+  f.bonus_token = bonus_token;
+  f.accept_rate = accept_rate;
+  f.kl_row = kl_row;
+  f.ce_row = ce_row;
+  f.ce_weight = ce_weight;
+  f.loss = loss;
+  f.status = d_status;
+  ADAFLASH_CUDA(launch_finalize(f, s));
+  return ADAFLASH_OK;
+}
+
+adaflash_status adaflash_opd_loss_bwd(const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
+                                      const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
+                                      const int32_t* draft_offsets, int32_t num_requests, int32_t num_draft_rows,
+                                      int32_t vocab, float clip_c, float ce_weight, const int32_t* target_argmax,
+                                      const float* row_stats, const float* grad_row, float grad_scale,
+                                      float* grad_draft, int64_t ld_g, uint32_t* d_status, void* stream) {
+  ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  ADAFLASH_TRY(check_logits(draft_logits, d_dtype, ld_d, vocab));
+  ADAFLASH_TRY(check_logits(target_logits, t_dtype, ld_t, vocab));
+  if (!int_ptr_ok(draft_offsets) || !int_ptr_ok(target_argmax) || !int_ptr_ok(row_stats) ||
+      !int_ptr_ok(grad_draft) || ld_g < vocab)
+    return ADAFLASH_ERR_INVALID_ARG;
+  if (grad_row && !aligned(grad_row, 4)) return ADAFLASH_ERR_INVALID_ARG;
+  if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
+  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight) || !std::isfinite(grad_scale)) return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_device());
+  if (num_requests == 0) return ADAFLASH_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  BwdParams p = {};
+  p.z = draft_logits;
+  p.t = target_logits;
+  p.ld_z = ld_d;
+  p.ld_t = ld_t;
+  p.doff = draft_offsets;
+  p.R = num_requests;
+  p.N_d = num_draft_rows;
+  p.N_t = num_draft_rows + num_requests;
+  p.V = vocab;
+  p.clip_c = clip_c;
+  p.ce_weight = ce_weight;
+  p.target_argmax = target_argmax;
+  p.row_stats = row_stats;
+  p.grad_row = grad_row;
+  p.grad_scale = grad_scale;
+  p.grad = grad_draft;
+  p.ld_g = ld_g;
+  p.chunks_per_row = (vocab + kBwdChunk - 1) / kBwdChunk;
+  p.status = d_status;
+  const bool fast = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
+                    rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)) && rows_16b(grad_draft, ld_g, 4);
+  ADAFLASH_CUDA(launch_bwd(p, d_dtype, t_dtype, fast, s));
+  return ADAFLASH_OK;
+}
+
+adaflash_status adaflash_selftest_bounded_wait(uint32_t* d_status, int32_t limit_us, void* stream) {
+  if (!int_ptr_ok(d_status) || limit_us < 1 || limit_us > 1000000) return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_device());
+  ADAFLASH_CUDA(launch_selftest_wait(d_status, limit_us, static_cast<cudaStream_t>(stream)));
+  return ADAFLASH_OK;
+}
+
+}  // extern "C"

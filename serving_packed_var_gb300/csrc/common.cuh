@@ -1,0 +1,194 @@
+// common.cuh -- device helpers shared by the kernels of the packed verify + OPD pass.
+//
+// Hand-written for sm_103a (GB300): bfloat16 unpacking, the MUFU base-2 exponential,
+// mbarrier / bulk-copy (TMA engine) wrappers with bounded waits, cluster barriers,
+// and the per-entry term of the clipped reverse KL that the forward screen and the
+// backward both evaluate with the same instruction sequence.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/adaflash.h"
+
+namespace adaflash {
+
+// log2(e) as a float; exponentials are computed as 2^(x * log2 e).
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Bounded waits give up after this many nanoseconds of %globaltimer.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------------------
+// status bits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void flag_status(uint32_t* status, int code) {
+  if (status) atomicOr(status, 1u << code);
+}
+
+// ---------------------------------------------------------------------------
+// element types
+// ---------------------------------------------------------------------------
+struct F32 {
+  using T = float;
+  static constexpr int kBytes = 4;
+  __device__ __forceinline__ static float load(const void* base, int64_t i) {
+    return __ldg(reinterpret_cast<const float*>(base) + i);
+  }
+};
+struct BF16 {
+  using T = uint16_t;
+  static constexpr int kBytes = 2;
+  __device__ __forceinline__ static float load(const void* base, int64_t i) {
+    const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(base) + i);
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// 2^x on the MUFU unit (flush-to-zero; 2^-inf = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------------------
+// the per-entry term of the clipped reverse KL
+// ---------------------------------------------------------------------------
+// p_v = exp(z_v - lse_z), r_v = (z_v - t_v) - (lse_z - lse_t), term_v = p_v r_v.
+// Written with explicit round-to-nearest intrinsics so that the forward's clip
+// screen and the backward reach the same clip decision bit for bit.
+struct TermConsts {
+  float neg_lse_z_l2e;  // -lse_z * log2 e
+  float dlse;           // lse_z - lse_t (float32 difference of the stored values)
+};
+
+__device__ __forceinline__ TermConsts make_term_consts(float lse_z, float lse_t) {
+  TermConsts c;
+  c.neg_lse_z_l2e = __fmul_rn(-lse_z, kLog2e);
+  c.dlse = __fsub_rn(lse_z, lse_t);
+  return c;
+}
+
+__device__ __forceinline__ void entry_term(float z, float t, const TermConsts& k, float& p, float& r,
+                                           float& term) {
+  p = ex2(__fmaf_rn(z, kLog2e, k.neg_lse_z_l2e));
+  r = __fsub_rn(__fsub_rn(z, t), k.dlse);
+  term = __fmul_rn(p, r);
+}
+
+// ---------------------------------------------------------------------------
+// time, mbarriers, bulk copies, cluster barriers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async proxy and the cluster.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after limit_ns.
+// Returns false on timeout; the caller reports ADAFLASH_ERR_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// One-dimensional bulk copy global -> this CTA's shared memory on the TMA engine;
+// completion is signalled as transaction bytes on `bar`.  dst, src and bytes must
+// be multiples of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  cluster_arrive_release();
+  cluster_wait_acquire();
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Generic address of the same shared-memory variable in CTA `rank` of the cluster.
+template <typename T>
+__device__ __forceinline__ T* map_to_rank(T* local, uint32_t rank) {
+  uint64_t out;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+  return reinterpret_cast<T*>(out);
+}
+
+// Request owning draft row d: the largest i in [0, R) with doff[i] <= d.
+__device__ __forceinline__ int request_of_row(const int32_t* doff, int R, int d) {
+  int lo = 0, hi = R - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(doff + mid) <= d) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace adaflash

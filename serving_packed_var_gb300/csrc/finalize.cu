@@ -1,0 +1,107 @@
+// finalize.cu -- K2: per-request greedy acceptance over the packed offsets, and the
+// batch loss as a fixed-order float64 sum.
+//
+// Greedy acceptance (AdaFlash article, opening section: the target verifies the
+// drafted block in parallel): with a_j the target's choice at the position of
+// draft token j, L_i is the first j whose token differs from a_j (k_i if none),
+// the bonus token is the target's choice at the position right after the accepted
+// prefix, and the acceptance rate L_i / k_i is the length head's free label
+// (section "2. Adaptive Length Head for Token-Level Variance").  One warp handles
+// one request: k_i <= 16 fits in one ballot.
+//
+// The loss is the mean over draft rows of kl + ce_weight * ce (the "mixture
+// reverse-KL loss" of the AdaFlash README, "Released Checkpoint").
+#include "common.cuh"
+#include "kernels.h"
+
+namespace adaflash {
+
+namespace {
+constexpr int kFinThreads = 1024;
+}
+
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeParams P) {
+  const int lane = threadIdx.x & 31;
+  const int gwarp = (blockIdx.x * kFinThreads + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * kFinThreads) >> 5;
+
+  for (int i = gwarp; i < P.R; i += nwarps) {
+    const int d0 = __ldg(P.doff + i);
+    const int d1 = __ldg(P.doff + i + 1);
+    const int k = d1 - d0;
+    bool ok = (k >= 1) && (k <= ADAFLASH_MAX_K) && (d0 >= 0) && (d1 <= P.N_d);
+    if (i == 0 && d0 != 0) ok = false;
+    if (i == P.R - 1 && d1 != P.N_d) ok = false;
+    if (!ok) {
+      if (lane == 0) {
+        P.accept_len[i] = -1;
+        P.bonus_token[i] = -1;
+        P.accept_rate[i] = -1.0f;
+        flag_status(P.status, ADAFLASH_ERR_BAD_OFFSETS);
+      }
+      continue;
+    }
+    bool mismatch = false, badtok = false;
+    if (lane < k) {
+      const int tok = __ldg(P.tokens + d0 + lane);
+      const int a = __ldg(P.target_argmax + d0 + i + lane);
+      badtok = (tok < 0) || (tok >= P.V);
+      mismatch = badtok || (tok != a);
+    }
+    const unsigned mm = __ballot_sync(0xffffffffu, mismatch);
+    const unsigned bt = __ballot_sync(0xffffffffu, badtok);
+    if (lane == 0) {
+      const int L = mm ? (__ffs(mm) - 1) : k;
+      P.accept_len[i] = L;
+      P.bonus_token[i] = __ldg(P.target_argmax + d0 + i + L);
+      P.accept_rate[i] = __fdiv_rn(static_cast<float>(L), static_cast<float>(k));
+      if (bt) flag_status(P.status, ADAFLASH_ERR_BAD_TOKEN);
+    }
+  }
+
+  if (P.kl_row == nullptr || blockIdx.x != 0) return;
+
+  // Fixed-order float64 reduction: strided partial sums, then a tree in shared memory.
+  __shared__ double part[kFinThreads];
+  double acc = 0.0;
+  for (int r = threadIdx.x; r < P.N_d; r += kFinThreads)
+    acc += static_cast<double>(P.kl_row[r]) + static_cast<double>(P.ce_weight) * static_cast<double>(P.ce_row[r]);
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = kFinThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) P.loss[0] = P.N_d > 0 ? static_cast<float>(part[0] / P.N_d) : 0.0f;
+}
+
+cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s) {
+  const int warps_per_block = kFinThreads / 32;
+  int blocks = (p.R + warps_per_block - 1) / warps_per_block;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 1024) blocks = 1024;
+  finalize_kernel<<<blocks, kFinThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// bounded-wait self-test: a barrier nothing completes, a wait that must give up
+// ---------------------------------------------------------------------------
+__global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // Phase 0 never completes: nobody arrives.
+  const bool ok = mbar_wait_bounded(&bar, 0, limit_ns);
+  if (!ok && threadIdx.x == 0) flag_status(status, ADAFLASH_ERR_TIMEOUT);
+}
+
+cudaError_t launch_selftest_wait(uint32_t* status, int32_t limit_us, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(status, static_cast<uint64_t>(limit_us) * 1000ull);
+  return cudaGetLastError();
+}
+
+}  // namespace adaflash

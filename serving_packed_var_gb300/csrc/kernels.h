@@ -1,0 +1,74 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace adaflash {
+
+enum RowPassMode : int32_t {
+  kModeVerify = 0,  // every target row is a target-only unit (argmax only)
+  kModeFwd = 1,     // draft rows are paired units, bonus target rows are target-only units
+};
+
+struct RowPassParams {
+  const void* z;  // draft logits [N_d, ld_z]
+  const void* t;  // target logits [N_t, ld_t]
+  int64_t ld_z, ld_t;
+  const int32_t* doff;
+  int32_t R, N_d, N_t, V;
+  int32_t mode;
+  int32_t cluster;  // CTAs per row unit (1..8)
+  int32_t slice;    // vocabulary entries per CTA (multiple of 8)
+  float clip_c;
+  int32_t* target_argmax;
+  float* kl_row;
+  float* ce_row;
+  float* row_stats;
+  uint32_t* status;
+};
+
+struct FinalizeParams {
+  const int32_t* tokens;
+  const int32_t* doff;
+  const int32_t* target_argmax;
+  int32_t R, N_d, V;
+  int32_t* accept_len;
+  int32_t* bonus_token;
+  float* accept_rate;
+  const float* kl_row;  // NULL: no loss
+  const float* ce_row;
+  float ce_weight;
+  float* loss;
+  uint32_t* status;
+};
+
+struct BwdParams {
+  const void* z;
+  const void* t;
+  int64_t ld_z, ld_t;
+  const int32_t* doff;
+  int32_t R, N_d, N_t, V;
+  float clip_c, ce_weight;
+  const int32_t* target_argmax;
+  const float* row_stats;
+  const float* grad_row;
+  float grad_scale;
+  float* grad;
+  int64_t ld_g;
+  int32_t chunks_per_row;
+  uint32_t* status;
+};
+
+// dtype codes match adaflash_dtype (0 = fp32, 1 = bf16)
+cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
+cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
+cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
+cudaError_t launch_selftest_wait(uint32_t* status, int32_t limit_us, cudaStream_t s);
+
+// Geometry chosen for a vocabulary size (shared by host validation and launches).
+int rowpass_cluster_size(int vocab);
+int rowpass_slice(int vocab, int cluster);
+constexpr int kBwdChunk = 8192;  // vocabulary entries per backward CTA
+
+}  // namespace adaflash
