@@ -129,7 +129,9 @@ def row_forward(z: np.ndarray, t: np.ndarray, c: float, beta: float = 1.0) -> di
     loss_row = kl + beta * ce (the "mixture" loss of the AdaFlash README,
           "Released Checkpoint"; beta is a reading).
     Also returns lse_z, lse_t, the target argmax a, the number of clipped terms
-    and S = sum_v m_v p_v (r_v + 1) (the row constant of the gradient).
+    and S = sum_v m_v p_v (r_v + 1) (the row constant of the gradient), with
+    S_l1 = sum_v m_v p_v |r_v + 1|, the size of S's summands: S is a difference of
+    large sums when much mass is clipped, and its error is judged against S_l1.
     """
     z = np.asarray(z, dtype=np.float64)
     t = np.asarray(t, dtype=np.float64)
@@ -139,8 +141,9 @@ def row_forward(z: np.ndarray, t: np.ndarray, c: float, beta: float = 1.0) -> di
     ce = hard_label_ce(z, a)
     m = term <= c
     S = float(np.sum(np.where(m, p * (r + 1.0), 0.0)))
+    S_l1 = float(np.sum(np.where(m, p * np.abs(r + 1.0), 0.0)))
     return dict(kl=kl, ce=ce, loss_row=kl + beta * ce, lse_z=log_sum_exp(z), lse_t=log_sum_exp(t),
-                argmax=a, n_clipped=int(np.count_nonzero(~m)), S=S)
+                argmax=a, n_clipped=int(np.count_nonzero(~m)), S=S, S_l1=S_l1)
 
 
 def row_grad(z: np.ndarray, t: np.ndarray, c: float, beta: float, g: float = 1.0) -> np.ndarray:

@@ -46,11 +46,11 @@ constexpr int kChunk = 4096;  // entries of each tensor per stage
 constexpr int kMaxCluster = 8;
 
 struct __align__(16) SlicePartial {
-  double sz, szd, st;
-  float mz, mt, dmax;
+  double sz, szd, st;  // sums scaled by 2^{nz}, 2^{nt} (see Acc)
+  float nz, nt;        // exponent offsets actually used (float32 values, exact)
+  float mt, dmax;      // max of t (for the argmax), max of z - t
   int bidx;
   int err;
-  int pad;
 };
 
 struct __align__(16) SliceCorr {
@@ -67,18 +67,24 @@ struct RowConsts {
   int err;
 };
 
-// Per-thread running state.  mz/mt are running maxima; sz = sum e^{z-mz},
-// st = sum e^{t-mt}, szd = sum e^{z-mz} (z - t); nmz = -mz * log2 e.
+// Per-thread running state.  Sums are kept relative to the exponent offset that
+// is actually applied, nz = fl(-max(z) * log2 e):
+//   sz = sum_v 2^{z_v log2e + nz},  szd = sum_v 2^{z_v log2e + nz} (z_v - t_v),
+//   st = sum_v 2^{t_v log2e + nt}.
+// Combining partials with their exact float offsets (rather than the maxima)
+// keeps the rounding of -max*log2e out of the result.
 struct Acc {
-  float mz, sz, szd, nmz;
-  float mt, st, nmt;
+  float mz, nz, sz, szd;
+  float mt, nt, st;
   float dmax;
   int bidx;
 };
 
+constexpr float kPosInf = __builtin_huge_valf();
+
 __device__ __forceinline__ void acc_init(Acc& a) {
-  a.mz = kNegInf; a.sz = 0.f; a.szd = 0.f; a.nmz = 0.f;
-  a.mt = kNegInf; a.st = 0.f; a.nmt = 0.f;
+  a.mz = kNegInf; a.nz = kPosInf; a.sz = 0.f; a.szd = 0.f;
+  a.mt = kNegInf; a.nt = kPosInf; a.st = 0.f;
   a.dmax = kNegInf;
   a.bidx = INT_MAX;
 }
@@ -96,24 +102,26 @@ __device__ __forceinline__ int first_eq(const float x[8], float v, int n) {
 __device__ __forceinline__ void acc_pair(Acc& a, const float z[8], const float t[8], float vmz, float vmt,
                                          int n, int v0) {
   if (vmz > a.mz) {
-    const float f = ex2((a.mz - vmz) * kLog2e);
+    const float nn = __fmul_rn(-vmz, kLog2e);
+    const float f = ex2(nn - a.nz);
     a.sz *= f;
     a.szd *= f;
     a.mz = vmz;
-    a.nmz = -vmz * kLog2e;
+    a.nz = nn;
   }
   if (vmt > a.mt) {
-    const float f = ex2((a.mt - vmt) * kLog2e);
+    const float nn = __fmul_rn(-vmt, kLog2e);
+    const float f = ex2(nn - a.nt);
     a.st *= f;
     a.mt = vmt;
-    a.nmt = -vmt * kLog2e;
+    a.nt = nn;
     a.bidx = v0 + first_eq(t, vmt, n);
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if (j < n) {
-      const float ez = ex2(fmaf(z[j], kLog2e, a.nmz));
-      const float et = ex2(fmaf(t[j], kLog2e, a.nmt));
+      const float ez = ex2(fmaf(z[j], kLog2e, a.nz));
+      const float et = ex2(fmaf(t[j], kLog2e, a.nt));
       a.sz += ez;
       a.st += et;
       const float d = z[j] - t[j];
@@ -168,41 +176,44 @@ __device__ __forceinline__ void load_global(const void* row, int64_t v0, int n, 
 
 // Warp-level combine of two thread states (float32, fixed xor pattern).
 __device__ __forceinline__ void acc_merge(Acc& a, const Acc& b) {
-  const float mz = fmaxf(a.mz, b.mz);
-  const float fa = (a.mz == kNegInf) ? 0.f : ex2((a.mz - mz) * kLog2e);
-  const float fb = (b.mz == kNegInf) ? 0.f : ex2((b.mz - mz) * kLog2e);
+  const float nz = fminf(a.nz, b.nz);
+  const float fa = (a.nz == kPosInf) ? 0.f : ex2(nz - a.nz);
+  const float fb = (b.nz == kPosInf) ? 0.f : ex2(nz - b.nz);
   a.sz = a.sz * fa + b.sz * fb;
   a.szd = a.szd * fa + b.szd * fb;
-  a.mz = mz;
-  const float mt = fmaxf(a.mt, b.mt);
-  const float ga = (a.mt == kNegInf) ? 0.f : ex2((a.mt - mt) * kLog2e);
-  const float gb = (b.mt == kNegInf) ? 0.f : ex2((b.mt - mt) * kLog2e);
+  a.nz = nz;
+  a.mz = fmaxf(a.mz, b.mz);
+  const float nt = fminf(a.nt, b.nt);
+  const float ga = (a.nt == kPosInf) ? 0.f : ex2(nt - a.nt);
+  const float gb = (b.nt == kPosInf) ? 0.f : ex2(nt - b.nt);
   a.st = a.st * ga + b.st * gb;
+  a.nt = nt;
   if (b.mt > a.mt || (b.mt == a.mt && b.bidx < a.bidx)) a.bidx = b.bidx;
-  a.mt = mt;
+  a.mt = fmaxf(a.mt, b.mt);
   a.dmax = fmaxf(a.dmax, b.dmax);
 }
 
 __device__ __forceinline__ Acc shfl_acc(const Acc& a, int off) {
   Acc b;
   b.mz = __shfl_xor_sync(0xffffffffu, a.mz, off);
+  b.nz = __shfl_xor_sync(0xffffffffu, a.nz, off);
   b.sz = __shfl_xor_sync(0xffffffffu, a.sz, off);
   b.szd = __shfl_xor_sync(0xffffffffu, a.szd, off);
   b.mt = __shfl_xor_sync(0xffffffffu, a.mt, off);
+  b.nt = __shfl_xor_sync(0xffffffffu, a.nt, off);
   b.st = __shfl_xor_sync(0xffffffffu, a.st, off);
   b.dmax = __shfl_xor_sync(0xffffffffu, a.dmax, off);
   b.bidx = __shfl_xor_sync(0xffffffffu, a.bidx, off);
-  b.nmz = 0.f;
-  b.nmt = 0.f;
   return b;
 }
 
-// float64 combine of slice partials in a fixed order.
+// float64 combine of slice partials in a fixed order; offsets combine exactly.
 __device__ void combine_partials(const SlicePartial* parts, int n, SlicePartial& out) {
-  float mz = kNegInf, mt = kNegInf, dmax = kNegInf;
+  float nz = kPosInf, nt = kPosInf, mt = kNegInf, dmax = kNegInf;
   int bidx = INT_MAX, err = 0;
   for (int i = 0; i < n; ++i) {
-    mz = fmaxf(mz, parts[i].mz);
+    nz = fminf(nz, parts[i].nz);
+    nt = fminf(nt, parts[i].nt);
     dmax = fmaxf(dmax, parts[i].dmax);
     if (parts[i].mt > mt || (parts[i].mt == mt && parts[i].bidx < bidx)) bidx = parts[i].bidx;
     mt = fmaxf(mt, parts[i].mt);
@@ -210,18 +221,23 @@ __device__ void combine_partials(const SlicePartial* parts, int n, SlicePartial&
   }
   double sz = 0.0, szd = 0.0, st = 0.0;
   for (int i = 0; i < n; ++i) {
-    if (parts[i].mz != kNegInf) {
-      const double f = exp(static_cast<double>(parts[i].mz) - static_cast<double>(mz));
+    if (parts[i].nz != kPosInf) {
+      const double f = exp2(static_cast<double>(nz) - static_cast<double>(parts[i].nz));
       sz += parts[i].sz * f;
       szd += parts[i].szd * f;
     }
-    if (parts[i].mt != kNegInf) {
-      const double g = exp(static_cast<double>(parts[i].mt) - static_cast<double>(mt));
+    if (parts[i].nt != kPosInf) {
+      const double g = exp2(static_cast<double>(nt) - static_cast<double>(parts[i].nt));
       st += parts[i].st * g;
     }
   }
-  out.mz = mz; out.mt = mt; out.dmax = dmax; out.bidx = bidx; out.err = err;
+  out.nz = nz; out.nt = nt; out.mt = mt; out.dmax = dmax; out.bidx = bidx; out.err = err;
   out.sz = sz; out.szd = szd; out.st = st;
+}
+
+// log sum_v e^{x_v} from a sum kept relative to the exponent offset n (base 2).
+__device__ __forceinline__ double lse_from(double sum, float n) {
+  return -static_cast<double>(n) * 0.69314718055994530942 + log(sum);
 }
 
 }  // namespace
@@ -372,8 +388,8 @@ __global__ void __launch_bounds__(kThreads) rowpass_kernel(const RowPassParams P
     for (int off = 16; off > 0; off >>= 1) acc_merge(acc, shfl_acc(acc, off));
     if (lane == 0) {
       SlicePartial& w = warp_part[warp];
-      w.mz = acc.mz; w.sz = acc.sz; w.szd = acc.szd;
-      w.mt = acc.mt; w.st = acc.st; w.dmax = acc.dmax; w.bidx = acc.bidx; w.err = 0;
+      w.nz = acc.nz; w.sz = acc.sz; w.szd = acc.szd;
+      w.nt = acc.nt; w.st = acc.st; w.mt = acc.mt; w.dmax = acc.dmax; w.bidx = acc.bidx; w.err = 0;
     }
   }
   const int any_err = __syncthreads_or(err);
@@ -401,8 +417,8 @@ __global__ void __launch_bounds__(kThreads) rowpass_kernel(const RowPassParams P
     rc.argmax = all.bidx;
     rc.err = all.err;
     if (pair) {
-      const double lse_z = static_cast<double>(all.mz) + log(all.sz);
-      const double lse_t = static_cast<double>(all.mt) + log(all.st);
+      const double lse_z = lse_from(all.sz, all.nz);
+      const double lse_t = lse_from(all.st, all.nt);
       const double dlse = lse_z - lse_t;
       rc.lse_z = lse_z;
       rc.lse_t = lse_t;
@@ -449,10 +465,13 @@ __global__ void __launch_bounds__(kThreads) rowpass_kernel(const RowPassParams P
           const float zv = DZ::load(zrow, v0 + j);
           const float tv = DT::load(trow, v0 + j);
           float p, r, term;
-          entry_term(zv, tv, tc, p, r, term);
+          entry_term(zv, tv, tc, p, r, term);  // the backward's decision, bit for bit
           if (term > c) {
-            corr += static_cast<double>(term) - static_cast<double>(c);
-            sclip += static_cast<double>(p) * (static_cast<double>(r) + 1.0);
+            // the clipped amount itself in float64 from the float64 log-sum-exps
+            const double pd = exp(static_cast<double>(zv) - rc.lse_z);
+            const double rd = (static_cast<double>(zv) - static_cast<double>(tv)) - (rc.lse_z - rc.lse_t);
+            corr += pd * rd - static_cast<double>(c);
+            sclip += pd * (rd + 1.0);
             ++nclip;
           }
         }

@@ -5,6 +5,7 @@ Tolerances (GPU vs float64 oracle):
   argmax, accept_len, bonus_token, accept_rate, n_clipped  -- bit-exact
   kl_row, ce_row, loss  -- |d| <= 1e-4 |ref| + 1e-6 for float32 inputs,
                            |d| <= 2e-3 |ref| + 1e-5 when an input is bfloat16
+  row_stats S           -- the same, with |ref| replaced by |S| + sum_v m_v p_v |r_v + 1|
   grad                  -- |d| <= 1e-5 + 1e-3 |ref|   (upstream weight 1)
 """
 
@@ -157,7 +158,8 @@ def check_rows(run: GpuRun, per: dict, grads: dict | None = None):
         st = h["row_stats"][d]
         assert abs(st[0] - f["lse_z"]) <= 1e-5 * abs(f["lse_z"]) + 1e-5, ("lse_z", d, st[0], f["lse_z"])
         assert abs(st[1] - f["lse_t"]) <= 1e-5 * abs(f["lse_t"]) + 1e-5, ("lse_t", d, st[1], f["lse_t"])
-        assert abs(st[2] - f["S"]) <= rel * abs(f["S"]) + ab, ("S", d, st[2], f["S"])
+        # S = sum m p (r+1) can be a small difference of large sums: judged against its summands' size
+        assert abs(st[2] - f["S"]) <= rel * (abs(f["S"]) + f["S_l1"]) + ab, ("S", d, st[2], f["S"])
         assert int(st[3]) == f["n_clipped"], ("n_clipped", d, st[3], f["n_clipped"])
         assert h["target_argmax"][w.pair_target_row(d)] == f["argmax"], ("argmax", d)
     if grads:
