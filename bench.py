@@ -1,0 +1,417 @@
+"""Benchmark of the packed verify + OPD-loss pass on GB300.
+
+One step = the whole path over one batch: the fused verify + loss forward
+(row pass K1 + acceptance scan/loss K2) and the backward (K3), through the C ABI.
+Default workload: concurrency 128 (V = 151936, bf16 logits, 128 requests with
+k_i from a truncated geometric on 1..16, clip c = 0.5).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  Multi-GPU (torchrun): every rank processes its
+own batch (weak scaling, no data-path collective); time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "logit rows/s for fused verify + clipped reverse-KL fwd/bwd; % of HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "serving_packed_var_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernels are unchanged since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return {}
+    if rec.get("source_sha") != source_hash():
+        return {}
+    return rec.get("kernels", {})
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]), hw=f[5], hwt=f[6],
+                                 swt=f[7], pcap=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in busy:
+            if r["hw"].lower() == "active":
+                reasons.add("hw_slowdown")
+            if r["hwt"].lower() == "active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"].lower() == "active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"].lower() == "active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(busy),
+                "power_w_median": statistics.median(r["power"] for r in busy)}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (torchrun, one GPU per rank)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def workload_config(w):
+    return {
+        "workload": f"{w.name}: concurrency {w.num_requests}, V={w.vocab}, {w.d_dtype} draft / {w.t_dtype} target, "
+                    f"k_i truncated-geometric on 1..16, clip c={w.clip_c}, fwd+bwd",
+        "num_requests": w.num_requests, "draft_rows": w.num_draft_rows, "target_rows": w.num_target_rows,
+        "vocab": w.vocab, "input_dtype": w.d_dtype, "clip_c": w.clip_c, "ce_weight": w.ce_weight,
+        "l2": "inputs larger than L2 (no flush): forward reads and backward traffic exceed 129 MB",
+        "parallelism": "replica per GPU (weak scaling)",
+    }
+
+
+def algorithmic_bytes(w):
+    V = w.vocab
+    bz, bt = w.bytes_per_draft_elem, w.bytes_per_target_elem
+    fwd = (w.num_draft_rows * (bz + bt) + w.num_requests * bt) * V
+    bwd = w.num_draft_rows * (bz + bt + 4) * V
+    return fwd, bwd
+
+
+def cpu_baseline(b, budget_s=10.0):
+    """The oracle as it stands (forward + gradient per draft row) on a bounded row sample."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    w = b.w
+    cores = os.cpu_count() or 1
+
+    def one(d):
+        s = w.pair_target_row(d)
+        z, t = b.draft_f64(d), b.target_f64(s)
+        oracle.row_forward(z, t, w.clip_c, w.ce_weight)
+        oracle.row_grad(z, t, w.clip_c, w.ce_weight, 1.0)
+
+    rows, t0 = 0, time.perf_counter()
+    with ThreadPoolExecutor(cores) as ex:
+        while rows < w.num_draft_rows and time.perf_counter() - t0 < budget_s:
+            batch = list(range(rows, min(w.num_draft_rows, rows + 4 * cores)))
+            list(ex.map(one, batch))
+            rows += len(batch)
+    el = time.perf_counter() - t0
+    return {"value": rows / el, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} draft rows of the same workload, float64 forward + gradient per row, "
+                      f"{cores} threads, {el:.1f} s"}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import serving_packed_var_gb300 as af
+    from synth import make_workload, materialize
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from serving_packed_var_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    barrier()
+
+    w = make_workload(args.workload, seed=rank)
+    b = materialize(w)
+    Nd, R = w.num_draft_rows, w.num_requests
+
+    def dev_from(arr, dtype):
+        if dtype == "bf16":
+            return torch.from_numpy(arr.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(arr).to(dev)
+
+    z = dev_from(b.draft, w.d_dtype)
+    t = dev_from(b.target, w.t_dtype)
+    tok = torch.from_numpy(b.tokens).to(dev)
+    doff = torch.from_numpy(b.doff).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = None
+    grad = torch.empty((Nd, w.vocab), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        nonlocal out
+        out = af.adaflash_opd_loss_fwd(z, t, tok, doff, w.clip_c, w.ce_weight, out=out, status=status)
+        af.adaflash_opd_loss_bwd(z, t, doff, out["target_argmax"], out["row_stats"], w.clip_c, w.ce_weight,
+                                 grad_scale=1.0 / Nd, out=grad, status=status)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(K):
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            out = af.adaflash_opd_loss_fwd(z, t, tok, doff, w.clip_c, w.ce_weight, out=out, status=status)
+            e1.record(stream)
+            af.adaflash_opd_loss_bwd(z, t, doff, out["target_argmax"], out["row_stats"], w.clip_c, w.ce_weight,
+                                     grad_scale=1.0 / Nd, out=grad, status=status)
+            e2.record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_local = start.elapsed_time(stop)
+    ms = max_over_ranks(ms_local, dev if world > 1 else None)
+    fwd_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / K
+    bwd_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / K
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    # end to end: pinned host inputs -> device, step, verify outputs + loss back to host
+    e2e = run_e2e(args, b, w, dev, af, torch, np)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = hbm_peak()
+    fb, bb = algorithmic_bytes(w)
+    traffic = ncu_traffic()
+    fwd_gbs = fb / (fwd_ms * 1e-3) / 1e9
+    bwd_gbs = bb / (bwd_ms * 1e-3) / 1e9
+    kernels = {
+        "fwd_pass": {"kernels": "rowpass (K1) + finalize (K2)", "ms": fwd_ms, "bytes": fb, "achieved_gbs": fwd_gbs,
+                     "frac": fwd_gbs / peak, "rows_per_s": Nd / (fwd_ms * 1e-3)},
+        "bwd": {"kernels": "bwd (K3)", "ms": bwd_ms, "bytes": bb, "achieved_gbs": bwd_gbs, "frac": bwd_gbs / peak,
+                "rows_per_s": Nd / (bwd_ms * 1e-3)},
+    }
+    dom = "bwd" if bwd_ms >= fwd_ms else "fwd_pass"
+    tr_key = "bwd_kernel" if dom == "bwd" else "rowpass_kernel"
+    roofline = {"bound": "hbm", "achieved": kernels[dom]["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                "frac": kernels[dom]["frac"], "traffic": traffic.get(tr_key, {}).get("dram_bytes_per_launch"),
+                "kernel": kernels[dom]["kernels"], "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": kernels[dom]["bytes"]}
+    roofline_fwd = {"bound": "hbm", "achieved": fwd_gbs, "peak": peak, "unit": "GB/s", "frac": fwd_gbs / peak,
+                    "traffic": traffic.get("rowpass_kernel", {}).get("dram_bytes_per_launch"),
+                    "kernel": "fused verify + loss forward (K1 + K2)", "algorithmic_bytes_per_launch": fb}
+    value = world * Nd / (ms * 1e-3 / K)
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded; no datasets or weights)",
+        "config": workload_config(w), "roofline": roofline, "roofline_fwd": roofline_fwd, "kernels": kernels,
+        "e2e": e2e, "gpu_launches": 3 * K, "clocks": clk.summary(),
+        "cpu_baseline": cpu_baseline(b) if world == 1 or rank == 0 else None,
+        "impl": "ours",
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, b, w, dev, af, torch, np):
+    """Same step through the public API from pinned host buffers, copies inside the timed region."""
+    Nd = w.num_draft_rows
+    zh = torch.from_numpy(b.draft.view(np.int16) if w.d_dtype == "bf16" else b.draft).pin_memory()
+    th = torch.from_numpy(b.target.view(np.int16) if w.t_dtype == "bf16" else b.target).pin_memory()
+    tokh = torch.from_numpy(b.tokens).pin_memory()
+    doffh = torch.from_numpy(b.doff).pin_memory()
+    zd = torch.empty_like(zh, device=dev)
+    td = torch.empty_like(th, device=dev)
+    tokd = torch.empty_like(tokh, device=dev)
+    doffd = torch.empty_like(doffh, device=dev)
+    zv = zd.view(torch.bfloat16) if w.d_dtype == "bf16" else zd
+    tv = td.view(torch.bfloat16) if w.t_dtype == "bf16" else td
+    R = w.num_requests
+    res_h = {"accept_len": torch.empty(R, dtype=torch.int32).pin_memory(),
+             "bonus_token": torch.empty(R, dtype=torch.int32).pin_memory(),
+             "accept_rate": torch.empty(R, dtype=torch.float32).pin_memory(),
+             "loss": torch.empty(1, dtype=torch.float32).pin_memory()}
+    grad = torch.empty((Nd, w.vocab), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = None
+    bi = sum(x.numel() * x.element_size() for x in (zh, th, tokh, doffh))
+    bo = sum(x.numel() * x.element_size() for x in res_h.values())
+    steps = max(3, min(args.steps, 50))
+
+    def step():
+        nonlocal out
+        zd.copy_(zh, non_blocking=True)
+        td.copy_(th, non_blocking=True)
+        tokd.copy_(tokh, non_blocking=True)
+        doffd.copy_(doffh, non_blocking=True)
+        out = af.adaflash_opd_loss_fwd(zv, tv, tokd, doffd, w.clip_c, w.ce_weight, out=out, status=status)
+        af.adaflash_opd_loss_bwd(zv, tv, doffd, out["target_argmax"], out["row_stats"], w.clip_c, w.ce_weight,
+                                 grad_scale=1.0 / Nd, out=grad, status=status)
+        for k, v in res_h.items():
+            v.copy_(out[k], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    el = max_over_ranks(time.perf_counter() - t0, dev if int(os.environ.get("WORLD_SIZE", "1")) > 1 else None)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"value": world * Nd * steps / el, "unit": "rows/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "steps": steps, "ms_per_step": el / steps * 1e3}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from synth import make_workload, materialize
+    w = make_workload(args.workload, seed=0)
+    b = materialize(w)
+    base = None
+    for _ in range(args.warmup):
+        cpu_baseline(b, budget_s=1.0)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        base = cpu_baseline(b, budget_s=max(1.0, min(20.0, 120.0 / max(1, args.steps))))
+        vals.append(base["value"])
+    el = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el / max(1, args.steps) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": workload_config(w), "impl": "reference",
+            "cpu_baseline": dict(base, value=value),
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c128")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

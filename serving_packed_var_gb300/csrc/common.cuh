@@ -192,3 +192,74 @@ __device__ __forceinline__ int request_of_row(const int32_t* doff, int R, int d)
 }
 
 }  // namespace adaflash
+
+namespace adaflash {
+
+// Exact 2^k for integer k <= 127 (0 below the normal range).
+__device__ __forceinline__ float pow2i(int k) {
+  return k < -126 ? 0.0f : __int_as_float((k + 127) << 23);
+}
+
+// ln(q) for finite q > 0 in float64 without a library call: q = m 2^e with
+// m in [sqrt(1/2), sqrt(2)), ln m = 2 atanh(s) = 2 (s + s^3/3 + s^5/5 + ...),
+// s = (m - 1)/(m + 1), |s| <= 0.1716; ten odd terms leave a relative error
+// below 1e-17 (the series' next term).
+__device__ __forceinline__ double ln_series(double q) {
+  long long bits = __double_as_longlong(q);
+  int e = static_cast<int>((bits >> 52) & 0x7ff) - 1023;
+  double m = __longlong_as_double((bits & 0x000fffffffffffffLL) | 0x3ff0000000000000LL);  // [1, 2)
+  if (m > 1.4142135623730951) {
+    m *= 0.5;
+    e += 1;
+  }
+  const double s = (m - 1.0) / (m + 1.0);
+  const double s2 = s * s;
+  double poly = 1.0 / 21.0;
+  poly = fma(poly, s2, 1.0 / 19.0);
+  poly = fma(poly, s2, 1.0 / 17.0);
+  poly = fma(poly, s2, 1.0 / 15.0);
+  poly = fma(poly, s2, 1.0 / 13.0);
+  poly = fma(poly, s2, 1.0 / 11.0);
+  poly = fma(poly, s2, 1.0 / 9.0);
+  poly = fma(poly, s2, 1.0 / 7.0);
+  poly = fma(poly, s2, 1.0 / 5.0);
+  poly = fma(poly, s2, 1.0 / 3.0);
+  poly = fma(poly, s2, 1.0);
+  return static_cast<double>(e) * 0.69314718055994530942 + 2.0 * s * poly;
+}
+
+// Cluster-scope mbarrier helpers (arrive on a peer CTA's barrier; acquire-wait).
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t* local_bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local_bar)), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Named barrier over the first `count` threads of the CTA (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int count) {
+  asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");
+}
+
+}  // namespace adaflash
