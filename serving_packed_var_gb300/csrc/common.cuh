@@ -118,14 +118,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One test of phase `parity`; a thread whose phase is not complete is suspended
+// for up to hint_ns (it wakes as soon as the phase completes), so waiting threads
+// do not spin on the issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 1000000u) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -134,10 +137,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Returns false on timeout; the caller reports ADAFLASH_ERR_TIMEOUT.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const uint32_t hint = limit_ns < 1000000ull ? static_cast<uint32_t>(limit_ns) : 1000000u;
+  if (mbar_try_wait(bar, parity, hint)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, hint)) return true;
     if (global_ns() - t0 > limit_ns) return false;
   }
 }
@@ -200,34 +204,6 @@ __device__ __forceinline__ float pow2i(int k) {
   return k < -126 ? 0.0f : __int_as_float((k + 127) << 23);
 }
 
-// ln(q) for finite q > 0 in float64 without a library call: q = m 2^e with
-// m in [sqrt(1/2), sqrt(2)), ln m = 2 atanh(s) = 2 (s + s^3/3 + s^5/5 + ...),
-// s = (m - 1)/(m + 1), |s| <= 0.1716; ten odd terms leave a relative error
-// below 1e-17 (the series' next term).
-__device__ __forceinline__ double ln_series(double q) {
-  long long bits = __double_as_longlong(q);
-  int e = static_cast<int>((bits >> 52) & 0x7ff) - 1023;
-  double m = __longlong_as_double((bits & 0x000fffffffffffffLL) | 0x3ff0000000000000LL);  // [1, 2)
-  if (m > 1.4142135623730951) {
-    m *= 0.5;
-    e += 1;
-  }
-  const double s = (m - 1.0) / (m + 1.0);
-  const double s2 = s * s;
-  double poly = 1.0 / 21.0;
-  poly = fma(poly, s2, 1.0 / 19.0);
-  poly = fma(poly, s2, 1.0 / 17.0);
-  poly = fma(poly, s2, 1.0 / 15.0);
-  poly = fma(poly, s2, 1.0 / 13.0);
-  poly = fma(poly, s2, 1.0 / 11.0);
-  poly = fma(poly, s2, 1.0 / 9.0);
-  poly = fma(poly, s2, 1.0 / 7.0);
-  poly = fma(poly, s2, 1.0 / 5.0);
-  poly = fma(poly, s2, 1.0 / 3.0);
-  poly = fma(poly, s2, 1.0);
-  return static_cast<double>(e) * 0.69314718055994530942 + 2.0 * s * poly;
-}
-
 // Cluster-scope mbarrier helpers (arrive on a peer CTA's barrier; acquire-wait).
 __device__ __forceinline__ void mbar_arrive_remote(uint64_t* local_bar, uint32_t rank) {
   uint32_t remote;
@@ -235,14 +211,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint64_t* local_bar, uint32_t
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 1000000u) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -260,6 +236,46 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
 // Named barrier over the first `count` threads of the CTA (id 1; id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int count) {
   asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");
+}
+
+}  // namespace adaflash
+
+namespace adaflash {
+
+// Packed pairs of float32 in one 64-bit register (two lanes per instruction on the
+// FMA pipe: fma/add/sub .f32x2).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 }  // namespace adaflash

@@ -10,9 +10,9 @@
 //                     ring of shared-memory stages (mbarrier-signalled), running
 //                     ahead across unit boundaries;
 //   8 consumer warps: per 8-entry group, an online log-sum-exp of z and of t,
-//                     sum_v e^{z_v}(z_v - t_v), max_v (z_v - t_v), the lowest-
-//                     index argmax of t, and the group maximum of z kept in
-//                     shared memory as a screening code.
+//                     sum_v e^{z_v}(z_v - t_v) (packed f32x2 arithmetic), a bound
+//                     on max_v (z_v - t_v), the lowest-index argmax of t, and the
+//                     group maximum of z kept in shared memory as a screening code.
 //
 // Slice results meet over distributed shared memory (remote stores + remote
 // mbarrier arrivals, double-buffered by unit parity).  Every CTA combines them in
@@ -26,9 +26,11 @@
 // HBM once.
 //
 // Exponent offsets are integers in base 2 (n = -ceil(max * log2 e)), so every
-// rescale and every combine of partial sums multiplies by an exact power of two;
-// float64 is used for a handful of additions, two divisions and one series
-// logarithm per row (GB300 has little float64 throughput).
+// rescale and every combine of partial sums multiplies by an exact power of two.
+// Everything is float32: on GB300 one float64 warp-instruction holds the small
+// float64 pipe for a whole warp's worth of lanes, and the per-row tail of this
+// kernel runs on a single thread.  The difference of log-sum-exps is taken as
+// (n_t - n_z) ln 2 + ln(S_z / S_t), never as a difference of two large logs.
 //
 // Operations: AdaFlash article ("AdaFlash: Adaptive Speculative Decoding with
 // Online Self-Improvement for High-Concurrency LLM Inference"), sections
@@ -51,119 +53,166 @@ constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kStages = 4;
 constexpr int kChunk = 4096;  // entries of each tensor per stage
+constexpr int kGroupsPerThread = kChunk / 8 / 256;  // 8-entry groups per consumer thread per chunk
 constexpr int kMaxCluster = 8;
 constexpr int kNoOffset = 1 << 30;  // offset of an empty partial sum
-constexpr double kLn2 = 0.69314718055994530942;
+constexpr float kLn2 = 0.69314718055994530942f;
 
 struct __align__(16) SlicePartial {
-  double sz, szd, st;  // sums scaled by 2^{nz}, 2^{nz}, 2^{nt}
-  int nz, nt;          // integer base-2 exponent offsets
-  float mt, dmax;      // max of t (argmax value), max of z - t
-  int bidx;
+  float sz, szd, st;  // sums scaled by 2^{nz}, 2^{nz}, 2^{nt}
+  int nz, nt;         // integer base-2 exponent offsets
+  float mt, dmax;     // max of t, bound on max of z - t
+  int bgrp;           // first group holding the max of t
   int err;
 };
 
 struct __align__(16) SliceCorr {
-  double corr, sclip;
+  float corr, sclip;
   int nclip;
   int err;
 };
 
 struct RowConsts {
-  double lse_z, lse_t;
+  float lse_z, lse_t, dlse, kl_unclip;
   float theta;
-  float lse_z_f, lse_t_f;
   int argmax;
   int err;
   int stop;  // every consumer thread leaves the unit loop together when set
 };
 
-// Per-thread running state: sz = sum_v 2^{z_v log2e + nz}, szd = sum_v 2^{z_v log2e + nz} (z_v - t_v),
-// st = sum_v 2^{t_v log2e + nt}; nz, nt integers (nzf, ntf the same values as floats).
+// Per-thread running state.  Sums are kept relative to integer base-2 exponent
+// offsets nz, nt and split over two accumulators (even / odd entries):
+//   sz = sum_v 2^{z_v log2e + nz},  szd = sum_v 2^{z_v log2e + nz} (z_v - t_v),
+//   st = sum_v 2^{t_v log2e + nt}.
+// Offsets move lazily: only when a group maximum lands more than kHeadroom powers
+// of two above the offset (a thread's first group, practically never after), so
+// the rescale branch is uniform and rare.  The argmax of t is tracked without
+// branches as (max value, first group holding it); the index inside that group
+// is resolved once per row.  dmax bounds max_v (z_v - t_v) from above by
+// max over groups of (max z - min t): it only sets the clip screen's threshold,
+// where a larger bound can only add candidates.
+constexpr float kHeadroom = 32.f;
+
 struct Acc {
-  float mz, sz, szd, nzf;
-  float mt, st, ntf;
-  float dmax;
+  float sz0, sz1, szd0, szd1, st0, st1;
+  float nzf, ntf;    // offsets as floats (integer-valued)
+  float zlim, tlim;  // a group maximum above these moves the offset
+  float mt;          // max of t
+  float dmax;        // bound on max (z - t)
   int nz, nt;
-  int bidx;
+  int bgrp;          // first (row-global) group index holding mt
+};
+
+// Scalar form used once a thread's accumulators are folded (warp/CTA combine).
+struct AccS {
+  float sz, szd, st;
+  float mt, dmax;
+  int nz, nt;
+  int bgrp;
 };
 
 __device__ __forceinline__ void acc_init(Acc& a) {
-  a.mz = kNegInf; a.sz = 0.f; a.szd = 0.f; a.nzf = 0.f; a.nz = kNoOffset;
-  a.mt = kNegInf; a.st = 0.f; a.ntf = 0.f; a.nt = kNoOffset;
+  a.sz0 = a.sz1 = a.szd0 = a.szd1 = a.st0 = a.st1 = 0.f;
+  a.nzf = a.ntf = 0.f;
+  a.zlim = a.tlim = kNegInf;
+  a.mt = kNegInf;
   a.dmax = kNegInf;
-  a.bidx = INT_MAX;
+  a.nz = a.nt = kNoOffset;
+  a.bgrp = INT_MAX;
 }
 
-// Integer offset for a new maximum m: -ceil(m log2 e) (clamped; logits are finite).
+__device__ __forceinline__ AccS acc_fold(const Acc& a) {
+  AccS s;
+  s.sz = a.sz0 + a.sz1;
+  s.szd = a.szd0 + a.szd1;
+  s.st = a.st0 + a.st1;
+  s.mt = a.mt; s.dmax = a.dmax; s.nz = a.nz; s.nt = a.nt; s.bgrp = a.bgrp;
+  return s;
+}
+
+// Integer offset that maps a new maximum m to 2^{<= 0}: -ceil(m log2 e) (clamped; logits are finite).
 __device__ __forceinline__ int offset_for(float m) {
   const float x = fminf(fmaxf(m * kLog2e, -1048576.f), 1048576.f);
   return -static_cast<int>(ceilf(x));
 }
 
-// Lowest j < n with x[j] == v (some j holds it).
-__device__ __forceinline__ int first_eq(const float x[8], float v, int n) {
-  int j = n - 1;
-#pragma unroll
-  for (int jj = 6; jj >= 0; --jj)
-    if (jj < n - 1 && x[jj] == v) j = jj;
-  return j;
+__device__ __forceinline__ void rescale_z(Acc& a, float vmz) {
+  const int nn = offset_for(vmz);
+  const float f = pow2i(nn - a.nz);
+  a.sz0 *= f; a.sz1 *= f; a.szd0 *= f; a.szd1 *= f;
+  a.nz = nn;
+  a.nzf = static_cast<float>(nn);
+  a.zlim = (kHeadroom - a.nzf) * 0.69314718f;  // z log2e + nz > kHeadroom  <=>  z > (kHeadroom - nz) ln 2
 }
 
-// Paired group: z[0..n), t[0..n) of vocabulary entries v0.., with group maxima vmz, vmt.
+__device__ __forceinline__ void rescale_t(Acc& a, float vmt) {
+  const int nn = offset_for(vmt);
+  const float f = pow2i(nn - a.nt);
+  a.st0 *= f; a.st1 *= f;
+  a.nt = nn;
+  a.ntf = static_cast<float>(nn);
+  a.tlim = (kHeadroom - a.ntf) * 0.69314718f;
+}
+
+// Value given to the unused entries of a ragged group: finite, and so small that
+// 2^{x log2e + n} is 0 and z - t is 0.
+constexpr float kVoid = -1.0e30f;
+
+// Paired group of 8 entries, row-global group index grp (unused entries of z and t
+// hold kVoid).  vmz = max z, vmt = max t, vnt = min t over the valid entries.
 __device__ __forceinline__ void acc_pair(Acc& a, const float z[8], const float t[8], float vmz, float vmt,
-                                         int n, int v0) {
-  if (vmz > a.mz) {
-    a.mz = vmz;
-    const int nn = offset_for(vmz);
-    if (nn < a.nz) {
-      const float f = pow2i(nn - a.nz);
-      a.sz *= f;
-      a.szd *= f;
-      a.nz = nn;
-      a.nzf = static_cast<float>(nn);
-    }
-  }
-  if (vmt > a.mt) {
-    a.mt = vmt;
-    a.bidx = v0 + first_eq(t, vmt, n);
-    const int nn = offset_for(vmt);
-    if (nn < a.nt) {
-      a.st *= pow2i(nn - a.nt);
-      a.nt = nn;
-      a.ntf = static_cast<float>(nn);
-    }
-  }
+                                         float vnt, int grp) {
+  if (vmz > a.zlim) rescale_z(a, vmz);
+  if (vmt > a.tlim) rescale_t(a, vmt);
+  const bool nb = vmt > a.mt;
+  a.mt = fmaxf(a.mt, vmt);
+  a.bgrp = nb ? grp : a.bgrp;
+  a.dmax = fmaxf(a.dmax, vmz - vnt);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j < n) {
-      const float ez = ex2(fmaf(z[j], kLog2e, a.nzf));
-      const float et = ex2(fmaf(t[j], kLog2e, a.ntf));
-      a.sz += ez;
-      a.st += et;
-      const float d = z[j] - t[j];
-      a.szd = fmaf(ez, d, a.szd);
-      a.dmax = fmaxf(a.dmax, d);
-    }
+  for (int q = 0; q < 4; ++q) {
+    const float ez0 = ex2(fmaf(z[2 * q], kLog2e, a.nzf));
+    const float ez1 = ex2(fmaf(z[2 * q + 1], kLog2e, a.nzf));
+    const float et0 = ex2(fmaf(t[2 * q], kLog2e, a.ntf));
+    const float et1 = ex2(fmaf(t[2 * q + 1], kLog2e, a.ntf));
+    a.sz0 += ez0;
+    a.sz1 += ez1;
+    a.st0 += et0;
+    a.st1 += et1;
+    a.szd0 = fmaf(ez0, z[2 * q] - t[2 * q], a.szd0);
+    a.szd1 = fmaf(ez1, z[2 * q + 1] - t[2 * q + 1], a.szd1);
   }
 }
 
 // Target-only group: argmax only.
-__device__ __forceinline__ void acc_target(Acc& a, const float t[8], float vmt, int n, int v0) {
-  if (vmt > a.mt) {
-    a.mt = vmt;
-    a.bidx = v0 + first_eq(t, vmt, n);
-  }
+__device__ __forceinline__ void acc_target(Acc& a, float vmt, int grp) {
+  const bool nb = vmt > a.mt;
+  a.mt = fmaxf(a.mt, vmt);
+  a.bgrp = nb ? grp : a.bgrp;
 }
 
+// Lowest index of the value mt inside group grp of a target row (-1 if absent).
 template <class DT>
-__device__ __forceinline__ void load8_smem(const uint8_t* base, int g, float x[8], float& vmax);
+__device__ int resolve_argmax(const uint8_t* trow, int grp, float mt, int V) {
+  if (grp < 0 || grp >= (V + 7) / 8) return -1;
+  const int v0 = grp * 8;
+  const int n = min(8, V - v0);
+  for (int j = 0; j < n; ++j)
+    if (DT::load(trow, v0 + j) == mt) return v0 + j;
+  return -1;
+}
+
+// Group of 8 from a shared-memory stage (16-byte aligned): values, max and min.
+template <class DT>
+__device__ __forceinline__ void load8_smem(const uint8_t* base, int g, float x[8], float& vmax, float& vmin);
 
 template <>
-__device__ __forceinline__ void load8_smem<BF16>(const uint8_t* base, int g, float x[8], float& vmax) {
+__device__ __forceinline__ void load8_smem<BF16>(const uint8_t* base, int g, float x[8], float& vmax,
+                                                 float& vmin) {
   const uint4 q = *reinterpret_cast<const uint4*>(base + 16 * g);
   const uint32_t m = bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w));
+  const uint32_t mn = bf16x2_min(bf16x2_min(q.x, q.y), bf16x2_min(q.z, q.w));
   vmax = fmaxf(bf16_lo(m), bf16_hi(m));
+  vmin = fminf(bf16_lo(mn), bf16_hi(mn));
   x[0] = bf16_lo(q.x); x[1] = bf16_hi(q.x);
   x[2] = bf16_lo(q.y); x[3] = bf16_hi(q.y);
   x[4] = bf16_lo(q.z); x[5] = bf16_hi(q.z);
@@ -171,83 +220,97 @@ __device__ __forceinline__ void load8_smem<BF16>(const uint8_t* base, int g, flo
 }
 
 template <>
-__device__ __forceinline__ void load8_smem<F32>(const uint8_t* base, int g, float x[8], float& vmax) {
+__device__ __forceinline__ void load8_smem<F32>(const uint8_t* base, int g, float x[8], float& vmax,
+                                                float& vmin) {
   const float4 a = *reinterpret_cast<const float4*>(base + 32 * g);
   const float4 b = *reinterpret_cast<const float4*>(base + 32 * g + 16);
   x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
   x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
   vmax = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
+  vmin = fminf(fminf(fminf(a.x, a.y), fminf(a.z, a.w)), fminf(fminf(b.x, b.y), fminf(b.z, b.w)));
 }
 
-// Up to 8 entries straight from global memory (any alignment).
+// Up to 8 entries straight from global memory (any alignment); unused entries get kVoid.
 template <class DT>
-__device__ __forceinline__ void load_global(const void* row, int64_t v0, int n, float x[8], float& vmax) {
+__device__ __forceinline__ void load_global(const void* row, int64_t v0, int n, float x[8], float& vmax,
+                                            float& vmin) {
   vmax = kNegInf;
+  vmin = -kNegInf;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    x[j] = (j < n) ? DT::load(row, v0 + j) : kNegInf;
-    vmax = fmaxf(vmax, x[j]);
+    if (j < n) {
+      x[j] = DT::load(row, v0 + j);
+      vmax = fmaxf(vmax, x[j]);
+      vmin = fminf(vmin, x[j]);
+    } else {
+      x[j] = kVoid;
+    }
   }
 }
 
 // Warp-level combine of two thread states (exact power-of-two rescaling).
-__device__ __forceinline__ void acc_merge(Acc& a, const Acc& b) {
+__device__ __forceinline__ void acc_merge(AccS& a, const AccS& b) {
   const int nz = min(a.nz, b.nz);
   const float fa = pow2i(nz - a.nz), fb = pow2i(nz - b.nz);
   a.sz = a.sz * fa + b.sz * fb;
   a.szd = a.szd * fa + b.szd * fb;
   a.nz = nz;
-  a.mz = fmaxf(a.mz, b.mz);
   const int nt = min(a.nt, b.nt);
   a.st = a.st * pow2i(nt - a.nt) + b.st * pow2i(nt - b.nt);
   a.nt = nt;
-  if (b.mt > a.mt || (b.mt == a.mt && b.bidx < a.bidx)) a.bidx = b.bidx;
+  if (b.mt > a.mt || (b.mt == a.mt && b.bgrp < a.bgrp)) a.bgrp = b.bgrp;
   a.mt = fmaxf(a.mt, b.mt);
   a.dmax = fmaxf(a.dmax, b.dmax);
 }
 
-__device__ __forceinline__ Acc shfl_acc(const Acc& a, int off) {
-  Acc b;
-  b.mz = __shfl_xor_sync(0xffffffffu, a.mz, off);
+__device__ __forceinline__ AccS shfl_acc(const AccS& a, int off) {
+  AccS b;
   b.sz = __shfl_xor_sync(0xffffffffu, a.sz, off);
   b.szd = __shfl_xor_sync(0xffffffffu, a.szd, off);
   b.nz = __shfl_xor_sync(0xffffffffu, a.nz, off);
-  b.mt = __shfl_xor_sync(0xffffffffu, a.mt, off);
   b.st = __shfl_xor_sync(0xffffffffu, a.st, off);
   b.nt = __shfl_xor_sync(0xffffffffu, a.nt, off);
+  b.mt = __shfl_xor_sync(0xffffffffu, a.mt, off);
   b.dmax = __shfl_xor_sync(0xffffffffu, a.dmax, off);
-  b.bidx = __shfl_xor_sync(0xffffffffu, a.bidx, off);
-  b.nzf = 0.f;
-  b.ntf = 0.f;
+  b.bgrp = __shfl_xor_sync(0xffffffffu, a.bgrp, off);
   return b;
 }
 
-// Fixed-order float64 combine of partials (exact power-of-two scaling).
+// Fixed-order combine of partials; the power-of-two factors are exact.
 __device__ void combine_partials(const SlicePartial* parts, int n, SlicePartial& out) {
-  int nz = kNoOffset, nt = kNoOffset, bidx = INT_MAX, err = 0;
+  int nz = kNoOffset, nt = kNoOffset, bgrp = INT_MAX, err = 0;
   float mt = kNegInf, dmax = kNegInf;
   for (int i = 0; i < n; ++i) {
     nz = min(nz, parts[i].nz);
     nt = min(nt, parts[i].nt);
     dmax = fmaxf(dmax, parts[i].dmax);
-    if (parts[i].mt > mt || (parts[i].mt == mt && parts[i].bidx < bidx)) bidx = parts[i].bidx;
+    if (parts[i].mt > mt || (parts[i].mt == mt && parts[i].bgrp < bgrp)) bgrp = parts[i].bgrp;
     mt = fmaxf(mt, parts[i].mt);
     err |= parts[i].err;
   }
-  double sz = 0.0, szd = 0.0, st = 0.0;
+  float sz = 0.f, szd = 0.f, st = 0.f;
   for (int i = 0; i < n; ++i) {
-    const double f = static_cast<double>(pow2i(nz - parts[i].nz));
-    sz += parts[i].sz * f;
-    szd += parts[i].szd * f;
-    st += parts[i].st * static_cast<double>(pow2i(nt - parts[i].nt));
+    const float f = pow2i(nz - parts[i].nz);
+    sz = fmaf(parts[i].sz, f, sz);
+    szd = fmaf(parts[i].szd, f, szd);
+    st = fmaf(parts[i].st, pow2i(nt - parts[i].nt), st);
   }
-  out.nz = nz; out.nt = nt; out.mt = mt; out.dmax = dmax; out.bidx = bidx; out.err = err;
+  out.nz = nz; out.nt = nt; out.mt = mt; out.dmax = dmax; out.bgrp = bgrp; out.err = err;
   out.sz = sz; out.szd = szd; out.st = st;
 }
 
-// log sum e^x at float accuracy from a positive sum kept relative to offset n.
-__device__ __forceinline__ double lse_approx(double sum, int n) {
-  return -static_cast<double>(n) * kLn2 + static_cast<double>(logf(static_cast<float>(sum)));
+// Row constants from the combined partials, all in float32:
+//   lse   = -n ln2 + ln(S)                     (offsets are integers: n ln2 is near-exact),
+//   dlse  = lse_z - lse_t = (nt - nz) ln2 + ln(Sz / St)   (no cancellation of two large logs),
+//   KL    = Szd / Sz - dlse.
+__device__ __forceinline__ void row_consts(const SlicePartial& all, RowConsts& rc) {
+  constexpr float kLn2Lo = -1.9046542e-09f;  // ln 2 - kLn2
+  const float nzf = static_cast<float>(all.nz), ntf = static_cast<float>(all.nt);
+  rc.lse_z = fmaf(-nzf, kLn2, fmaf(-nzf, kLn2Lo, logf(all.sz)));
+  rc.lse_t = fmaf(-ntf, kLn2, fmaf(-ntf, kLn2Lo, logf(all.st)));
+  const float dn = static_cast<float>(all.nt - all.nz);
+  rc.dlse = fmaf(dn, kLn2, fmaf(dn, kLn2Lo, logf(all.sz / all.st)));
+  rc.kl_unclip = all.szd / all.sz - rc.dlse;
 }
 
 struct Unit {
@@ -289,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
   __shared__ SlicePartial slots[2][kMaxCluster];
   __shared__ SliceCorr cslots[2][kMaxCluster];
   __shared__ SlicePartial warp_part[kConsumerWarps];
-  __shared__ double warp_corr[kConsumerWarps][2];
+  __shared__ float warp_corr[kConsumerWarps][2];
   __shared__ int warp_nclip[kConsumerWarps];
   __shared__ RowConsts rc;
   __shared__ int s_abort;
@@ -394,18 +457,28 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
           }
           const int gcount = min(kChunk, body - e0) >> 3;
           const uint8_t* stage = ring + st * (kStageZ + kStageT);
-          const int gbase = e0 >> 3;
-          for (int g = tid; g < gcount; g += kConsumers) {
-            float t[8], vmt;
-            load8_smem<DT>(stage + kStageZ, g, t, vmt);
-            const int v0 = v_begin + ((gbase + g) << 3);
-            if (U.pair) {
-              float z[8], vmz;
-              load8_smem<DZ>(stage, g, z, vmz);
-              codes[gbase + g] = vmz;
-              acc_pair(acc, z, t, vmz, vmt, 8, v0);
-            } else {
-              acc_target(acc, t, vmt, 8, v0);
+          const int gbase = (v_begin + e0) >> 3;  // row-global group index of the chunk's first group
+          if (U.pair) {
+#pragma unroll
+            for (int k = 0; k < kGroupsPerThread; ++k) {
+              const int g = tid + k * kConsumers;
+              if (g < gcount) {
+                float z[8], t[8], vmz, vnz, vmt, vnt;
+                load8_smem<DZ>(stage, g, z, vmz, vnz);
+                load8_smem<DT>(stage + kStageZ, g, t, vmt, vnt);
+                codes[(e0 >> 3) + g] = vmz;
+                acc_pair(acc, z, t, vmz, vmt, vnt, gbase + g);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kGroupsPerThread; ++k) {
+              const int g = tid + k * kConsumers;
+              if (g < gcount) {
+                float t[8], vmt, vnt;
+                load8_smem<DT>(stage + kStageZ, g, t, vmt, vnt);
+                acc_target(acc, vmt, gbase + g);
+              }
             }
           }
           __syncwarp();
@@ -416,25 +489,27 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
       for (int g = (body >> 3) + tid; g < ngroups; g += kConsumers) {
         const int64_t v0 = v_begin + (static_cast<int64_t>(g) << 3);
         const int n = min(8, v_end - static_cast<int>(v0));
-        float t[8], vmt;
-        load_global<DT>(trow, v0, n, t, vmt);
+        const int grp = static_cast<int>(v0 >> 3);
+        float t[8], vmt, vnt;
+        load_global<DT>(trow, v0, n, t, vmt, vnt);
         if (U.pair) {
-          float z[8], vmz;
-          load_global<DZ>(zrow, v0, n, z, vmz);
+          float z[8], vmz, vnz;
+          load_global<DZ>(zrow, v0, n, z, vmz, vnz);
           codes[g] = vmz;
-          acc_pair(acc, z, t, vmz, vmt, n, static_cast<int>(v0));
+          acc_pair(acc, z, t, vmz, vmt, vnt, grp);
         } else {
-          acc_target(acc, t, vmt, n, static_cast<int>(v0));
+          acc_target(acc, vmt, grp);
         }
       }
 
       // ---- CTA reduction, then the exchange of slice partials ----
+      AccS as = acc_fold(acc);
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc_merge(acc, shfl_acc(acc, off));
+      for (int off = 16; off > 0; off >>= 1) acc_merge(as, shfl_acc(as, off));
       if (lane == 0) {
         SlicePartial& w = warp_part[warp];
-        w.nz = acc.nz; w.sz = acc.sz; w.szd = acc.szd;
-        w.nt = acc.nt; w.st = acc.st; w.mt = acc.mt; w.dmax = acc.dmax; w.bidx = acc.bidx; w.err = 0;
+        w.nz = as.nz; w.sz = as.sz; w.szd = as.szd;
+        w.nt = as.nt; w.st = as.st; w.mt = as.mt; w.dmax = as.dmax; w.bgrp = as.bgrp; w.err = 0;
       }
       named_bar_sync(kConsumers);
 
@@ -453,26 +528,21 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
         }
         SlicePartial all;
         combine_partials(slots[buf], C, all);
-        rc.argmax = all.bidx;
+        // The lowest index of the maximum lies in the first group holding it.
+        rc.argmax = (rank == 0 && !U.bad) ? resolve_argmax<DT>(trow, all.bgrp, all.mt, P.V) : -1;
         rc.err = all.err | werr;
         rc.stop = *abort_flag;
         if (U.pair && !U.bad) {
-          const double lse_z = lse_approx(all.sz, all.nz);
-          const double lse_t = lse_approx(all.st, all.nt);
-          const float dlse = static_cast<float>(lse_z - lse_t);
-          rc.lse_z = lse_z;
-          rc.lse_t = lse_t;
-          rc.lse_z_f = static_cast<float>(lse_z);
-          rc.lse_t_f = static_cast<float>(lse_t);
+          row_consts(all, rc);
           // Screen threshold on group maxima of z; the slack only adds candidates.
-          const float R = all.dmax - dlse;
-          const float Rp = R + 1e-4f * (1.f + fabsf(all.dmax) + fabsf(dlse));
+          const float R = all.dmax - rc.dlse;
+          const float Rp = R + 1e-4f * (1.f + fabsf(all.dmax) + fabsf(rc.dlse));
           const float c = P.clip_c;
           if (!(c < INFINITY) || !(Rp > 0.f)) {
             rc.theta = INFINITY;
           } else {
-            const double th = lse_z + static_cast<double>(logf(c / Rp)) - (1e-3 + 1e-6 * fabs(lse_z));
-            rc.theta = __double2float_rd(th);
+            const float th = rc.lse_z + logf(c / Rp);
+            rc.theta = th - (1e-3f + 1e-5f * fabsf(th));
           }
         }
       }
@@ -482,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
       if (!U.pair) {
         if (rank == 0 && tid == 0) {
           if (U.bad) flag_status(P.status, ADAFLASH_ERR_BAD_OFFSETS);
+          else if (rc.argmax < 0 || rc.argmax >= P.V) flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
           else {
             P.target_argmax[U.s] = rc.argmax;
             if (rc.err) flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
@@ -492,11 +563,11 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
       }
 
       // ---- exact evaluation of the screened groups ----
-      double corr = 0.0, sclip = 0.0;
+      float corr = 0.f, sclip = 0.f;
       int nclip = 0;
       {
         const float theta = U.bad ? INFINITY : rc.theta;
-        const TermConsts tc = make_term_consts(rc.lse_z_f, rc.lse_t_f);
+        const TermConsts tc = make_term_consts(rc.lse_z, rc.lse_t);
         const float c = P.clip_c;
         for (int g = tid; g < ngroups; g += kConsumers) {
           if (codes[g] > theta) {
@@ -506,15 +577,10 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
               const float zv = DZ::load(zrow, v0 + j);
               const float tv = DT::load(trow, v0 + j);
               float p, r, term;
-              entry_term(zv, tv, tc, p, r, term);  // the backward's decision, bit for bit
+              entry_term(zv, tv, tc, p, r, term);  // the backward's evaluation, bit for bit
               if (term > c) {
-                // the clipped amount, from the log-sum-exps before float32 rounding
-                const double zd = static_cast<double>(zv);
-                const float arg = static_cast<float>((zd - rc.lse_z) * 1.4426950408889634);
-                const double pd = static_cast<double>(ex2(arg));
-                const double rd = (zd - static_cast<double>(tv)) - (rc.lse_z - rc.lse_t);
-                corr += pd * rd - static_cast<double>(c);
-                sclip += pd * (rd + 1.0);
+                corr += term - c;
+                sclip = fmaf(p, r + 1.f, sclip);
                 ++nclip;
               }
             }
@@ -536,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
       const int cbuf = pit & 1;
       if (tid == 0) {
         SliceCorr mine;
-        mine.corr = 0.0; mine.sclip = 0.0; mine.nclip = 0; mine.err = rc.err;
+        mine.corr = 0.f; mine.sclip = 0.f; mine.nclip = 0; mine.err = rc.err;
         for (int w = 0; w < kConsumerWarps; ++w) {
           mine.corr += warp_corr[w][0];
           mine.sclip += warp_corr[w][1];
@@ -549,8 +615,11 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
           if (!ok) *abort_flag = 1;
           if (U.bad) {
             flag_status(P.status, ADAFLASH_ERR_BAD_OFFSETS);
+          } else if (rc.argmax < 0 || rc.argmax >= P.V) {
+            // only after an aborted unit (no group was reduced): nothing valid to write
+            flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
           } else {
-            double corr_all = 0.0, sclip_all = 0.0;
+            float corr_all = 0.f, sclip_all = 0.f;
             int nclip_all = 0, err_all = rc.err | (ok ? 0 : 1);
             for (int r = 0; r < C; ++r) {
               corr_all += cslots[cbuf][r].corr;
@@ -558,19 +627,13 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
               nclip_all += cslots[cbuf][r].nclip;
               err_all |= cslots[cbuf][r].err;
             }
-            // Accurate difference of the log-sum-exps for the unclipped KL.
-            SlicePartial all;
-            combine_partials(slots[buf], C, all);
-            const double dlse = static_cast<double>(all.nt - all.nz) * kLn2 + ln_series(all.sz / all.st);
-            const double kl_unclip = all.szd / all.sz - dlse;
             const int a = rc.argmax;
-            const double z_a = static_cast<double>(DZ::load(zrow, a));
             const int64_t d = U.d;
-            P.kl_row[d] = static_cast<float>(kl_unclip - corr_all);
-            P.ce_row[d] = static_cast<float>(rc.lse_z - z_a);
-            P.row_stats[4 * d + 0] = rc.lse_z_f;
-            P.row_stats[4 * d + 1] = rc.lse_t_f;
-            P.row_stats[4 * d + 2] = static_cast<float>(kl_unclip + 1.0 - sclip_all);
+            P.kl_row[d] = rc.kl_unclip - corr_all;
+            P.ce_row[d] = rc.lse_z - DZ::load(zrow, a);
+            P.row_stats[4 * d + 0] = rc.lse_z;
+            P.row_stats[4 * d + 1] = rc.lse_t;
+            P.row_stats[4 * d + 2] = (rc.kl_unclip + 1.f) - sclip_all;
             P.row_stats[4 * d + 3] = static_cast<float>(nclip_all);
             P.target_argmax[U.s] = a;
             if (err_all) flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
