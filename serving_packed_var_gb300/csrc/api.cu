@@ -59,6 +59,18 @@ adaflash_status check_device() {
   return ok ? ADAFLASH_OK : ADAFLASH_ERR_UNSUPPORTED;
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms() {
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 152;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
 #define ADAFLASH_TRY(expr)                          \
   do {                                              \
     const adaflash_status st_ = (expr);             \
@@ -111,7 +123,7 @@ adaflash_status adaflash_verify_packed(const void* target_logits, adaflash_dtype
   p.N_t = num_draft_rows + num_requests;
   p.V = vocab;
   p.mode = kModeVerify;
-  p.cluster = rowpass_cluster_size(vocab);
+  p.cluster = rowpass_cluster_size(vocab, p.mode == kModeVerify ? p.N_t : p.N_d + p.R, num_sms());
   p.slice = rowpass_slice(vocab, p.cluster);
   p.clip_c = 1.0f;
   p.target_argmax = target_argmax;
@@ -168,7 +180,7 @@ adaflash_status adaflash_opd_loss_fwd(const void* draft_logits, adaflash_dtype d
   p.N_t = num_draft_rows + num_requests;
   p.V = vocab;
   p.mode = kModeFwd;
-  p.cluster = rowpass_cluster_size(vocab);
+  p.cluster = rowpass_cluster_size(vocab, p.mode == kModeVerify ? p.N_t : p.N_d + p.R, num_sms());
   p.slice = rowpass_slice(vocab, p.cluster);
   p.clip_c = clip_c;
   p.target_argmax = target_argmax;

@@ -233,6 +233,13 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
   }
 }
 
+// Warp-wide float max in one instruction (redux.sync, sm_100 family).
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 // Named barrier over the first `count` threads of the CTA (id 1; id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int count) {
   asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");

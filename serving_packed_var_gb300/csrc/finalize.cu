@@ -21,6 +21,9 @@ constexpr int kFinThreads = 1024;
 }
 
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeParams P) {
+  // Launched as a programmatic dependent of the row pass: wait until its writes
+  // (target_argmax, kl_row, ce_row) are complete and visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * kFinThreads + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * kFinThreads) >> 5;
@@ -61,18 +64,28 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
 
   if (P.kl_row == nullptr || blockIdx.x != 0) return;
 
-  // Fixed-order float64 reduction: strided partial sums, then a tree in shared memory.
-  __shared__ double part[kFinThreads];
-  double acc = 0.0;
-  for (int r = threadIdx.x; r < P.N_d; r += kFinThreads)
-    acc += static_cast<double>(P.kl_row[r]) + static_cast<double>(P.ce_weight) * static_cast<double>(P.ce_row[r]);
-  part[threadIdx.x] = acc;
-  __syncthreads();
-  for (int w = kFinThreads / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
-    __syncthreads();
+  // Fixed-order float32 reduction (GB300's float64 pipe is narrow): each thread
+  // sums a fixed strided subset with compensation (Kahan), then a fixed warp and
+  // block tree.  The order never changes, so the loss is bitwise reproducible;
+  // its relative error is about 1e-6, far below the loss tolerance.
+  __shared__ float part[kFinThreads / 32];
+  float acc = 0.f, comp = 0.f;
+  for (int r = threadIdx.x; r < P.N_d; r += kFinThreads) {
+    const float y = __fsub_rn(fmaf(P.ce_weight, P.ce_row[r], P.kl_row[r]), comp);
+    const float t = __fadd_rn(acc, y);
+    comp = __fsub_rn(__fsub_rn(t, acc), y);
+    acc = t;
   }
-  if (threadIdx.x == 0) P.loss[0] = P.N_d > 0 ? static_cast<float>(part[0] / P.N_d) : 0.0f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) part[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = part[threadIdx.x];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (threadIdx.x == 0) P.loss[0] = P.N_d > 0 ? v / static_cast<float>(P.N_d) : 0.0f;
+  }
 }
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s) {
@@ -80,8 +93,16 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s) {
   int blocks = (p.R + warps_per_block - 1) / warps_per_block;
   if (blocks < 1) blocks = 1;
   if (blocks > 1024) blocks = 1024;
-  finalize_kernel<<<blocks, kFinThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kFinThreads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, finalize_kernel, p);
 }
 
 // ---------------------------------------------------------------------------

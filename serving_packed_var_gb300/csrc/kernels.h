@@ -67,7 +67,7 @@ cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool fast, 
 cudaError_t launch_selftest_wait(uint32_t* status, int32_t limit_us, cudaStream_t s);
 
 // Geometry chosen for a vocabulary size (shared by host validation and launches).
-int rowpass_cluster_size(int vocab);
+int rowpass_cluster_size(int vocab, int units, int num_sms);
 int rowpass_slice(int vocab, int cluster);
 constexpr int kBwdChunk = 8192;  // vocabulary entries per backward CTA
 

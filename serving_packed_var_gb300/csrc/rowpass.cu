@@ -10,9 +10,9 @@
 //                     ring of shared-memory stages (mbarrier-signalled), running
 //                     ahead across unit boundaries;
 //   8 consumer warps: per 8-entry group, an online log-sum-exp of z and of t,
-//                     sum_v e^{z_v}(z_v - t_v) (packed f32x2 arithmetic), a bound
+//                     sum_v e^{z_v}(z_v - t_v), a bound
 //                     on max_v (z_v - t_v), the lowest-index argmax of t, and the
-//                     group maximum of z kept in shared memory as a screening code.
+//                     largest group maximum of z each thread sees.
 //
 // Slice results meet over distributed shared memory (remote stores + remote
 // mbarrier arrivals, double-buffered by unit parity).  Every CTA combines them in
@@ -20,8 +20,9 @@
 //     KL = sum_v p_v (z_v - t_v) - (lse_z - lse_t),
 // and the bound term_v = p_v r_v <= p_v R, R = max_v(z_v - t_v) - (lse_z - lse_t).
 // A term can exceed the clip c only where p_v > c / R, i.e. z_v > lse_z + log(c/R);
-// each CTA compares its group codes with that threshold (no exponentials) and
-// evaluates only the flagged groups exactly, re-reading those few entries.  The
+// each thread compares the largest group maximum of z it saw with that threshold
+// (no exponentials) and only when it is above, its groups are re-read and the ones
+// above the threshold evaluated exactly.  The
 // clipped KL is KL - sum_{term_v > c} (term_v - c): each logit byte is read from
 // HBM once.
 //
@@ -51,7 +52,15 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
-constexpr int kStages = 4;
+// Ring depth and resident CTAs per SM (compile-time tuning; the defaults are the
+// measured best on GB300 for bf16 logits).
+#ifndef ADAFLASH_ROWPASS_STAGES
+#define ADAFLASH_ROWPASS_STAGES 3
+#endif
+#ifndef ADAFLASH_ROWPASS_MINBLOCKS
+#define ADAFLASH_ROWPASS_MINBLOCKS 3
+#endif
+constexpr int kStages = ADAFLASH_ROWPASS_STAGES;
 constexpr int kChunk = 4096;  // entries of each tensor per stage
 constexpr int kGroupsPerThread = kChunk / 8 / 256;  // 8-entry groups per consumer thread per chunk
 constexpr int kMaxCluster = 8;
@@ -78,6 +87,7 @@ struct RowConsts {
   int argmax;
   int err;
   int stop;  // every consumer thread leaves the unit loop together when set
+  int scan;  // some thread of this CTA saw a group maximum of z above the threshold
 };
 
 // Per-thread running state.  Sums are kept relative to integer base-2 exponent
@@ -99,6 +109,7 @@ struct Acc {
   float zlim, tlim;  // a group maximum above these moves the offset
   float mt;          // max of t
   float dmax;        // bound on max (z - t)
+  float cmax;        // largest group maximum of z among this thread's groups
   int nz, nt;
   int bgrp;          // first (row-global) group index holding mt
 };
@@ -106,7 +117,7 @@ struct Acc {
 // Scalar form used once a thread's accumulators are folded (warp/CTA combine).
 struct AccS {
   float sz, szd, st;
-  float mt, dmax;
+  float mt, dmax, cmax;
   int nz, nt;
   int bgrp;
 };
@@ -117,6 +128,7 @@ __device__ __forceinline__ void acc_init(Acc& a) {
   a.zlim = a.tlim = kNegInf;
   a.mt = kNegInf;
   a.dmax = kNegInf;
+  a.cmax = kNegInf;
   a.nz = a.nt = kNoOffset;
   a.bgrp = INT_MAX;
 }
@@ -126,7 +138,7 @@ __device__ __forceinline__ AccS acc_fold(const Acc& a) {
   s.sz = a.sz0 + a.sz1;
   s.szd = a.szd0 + a.szd1;
   s.st = a.st0 + a.st1;
-  s.mt = a.mt; s.dmax = a.dmax; s.nz = a.nz; s.nt = a.nt; s.bgrp = a.bgrp;
+  s.mt = a.mt; s.dmax = a.dmax; s.cmax = a.cmax; s.nz = a.nz; s.nt = a.nt; s.bgrp = a.bgrp;
   return s;
 }
 
@@ -154,20 +166,29 @@ __device__ __forceinline__ void rescale_t(Acc& a, float vmt) {
   a.tlim = (kHeadroom - a.ntf) * 0.69314718f;
 }
 
+// Screening code: a group maximum of z rounded up to bfloat16 (exact for bf16
+// logits), so a code at or below a threshold proves every entry below it.
+__device__ __forceinline__ uint16_t code_up(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return static_cast<uint16_t>((v > 0.f ? b + 0xffffu : b) >> 16);
+}
+__device__ __forceinline__ float code_value(uint16_t c) { return __uint_as_float(static_cast<uint32_t>(c) << 16); }
+
 // Value given to the unused entries of a ragged group: finite, and so small that
 // 2^{x log2e + n} is 0 and z - t is 0.
 constexpr float kVoid = -1.0e30f;
 
 // Paired group of 8 entries, row-global group index grp (unused entries of z and t
-// hold kVoid).  vmz = max z, vmt = max t, vnt = min t over the valid entries.
+// hold kVoid).  vmz = max z, vmt = max t over the valid entries.
 __device__ __forceinline__ void acc_pair(Acc& a, const float z[8], const float t[8], float vmz, float vmt,
-                                         float vnt, int grp) {
+                                         int grp) {
   if (vmz > a.zlim) rescale_z(a, vmz);
   if (vmt > a.tlim) rescale_t(a, vmt);
   const bool nb = vmt > a.mt;
   a.mt = fmaxf(a.mt, vmt);
   a.bgrp = nb ? grp : a.bgrp;
-  a.dmax = fmaxf(a.dmax, vmz - vnt);
+  a.cmax = fmaxf(a.cmax, vmz);
+  float dm0 = a.dmax, dm1 = kNegInf;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const float ez0 = ex2(fmaf(z[2 * q], kLog2e, a.nzf));
@@ -178,9 +199,13 @@ __device__ __forceinline__ void acc_pair(Acc& a, const float z[8], const float t
     a.sz1 += ez1;
     a.st0 += et0;
     a.st1 += et1;
-    a.szd0 = fmaf(ez0, z[2 * q] - t[2 * q], a.szd0);
-    a.szd1 = fmaf(ez1, z[2 * q + 1] - t[2 * q + 1], a.szd1);
+    const float d0 = z[2 * q] - t[2 * q], d1 = z[2 * q + 1] - t[2 * q + 1];
+    a.szd0 = fmaf(ez0, d0, a.szd0);
+    a.szd1 = fmaf(ez1, d1, a.szd1);
+    dm0 = fmaxf(dm0, d0);
+    dm1 = fmaxf(dm1, d1);
   }
+  a.dmax = fmaxf(dm0, dm1);
 }
 
 // Target-only group: argmax only.
@@ -203,16 +228,13 @@ __device__ int resolve_argmax(const uint8_t* trow, int grp, float mt, int V) {
 
 // Group of 8 from a shared-memory stage (16-byte aligned): values, max and min.
 template <class DT>
-__device__ __forceinline__ void load8_smem(const uint8_t* base, int g, float x[8], float& vmax, float& vmin);
+__device__ __forceinline__ void load8_smem(const uint8_t* base, int g, float x[8], float& vmax);
 
 template <>
-__device__ __forceinline__ void load8_smem<BF16>(const uint8_t* base, int g, float x[8], float& vmax,
-                                                 float& vmin) {
+__device__ __forceinline__ void load8_smem<BF16>(const uint8_t* base, int g, float x[8], float& vmax) {
   const uint4 q = *reinterpret_cast<const uint4*>(base + 16 * g);
   const uint32_t m = bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w));
-  const uint32_t mn = bf16x2_min(bf16x2_min(q.x, q.y), bf16x2_min(q.z, q.w));
   vmax = fmaxf(bf16_lo(m), bf16_hi(m));
-  vmin = fminf(bf16_lo(mn), bf16_hi(mn));
   x[0] = bf16_lo(q.x); x[1] = bf16_hi(q.x);
   x[2] = bf16_lo(q.y); x[3] = bf16_hi(q.y);
   x[4] = bf16_lo(q.z); x[5] = bf16_hi(q.z);
@@ -220,60 +242,51 @@ __device__ __forceinline__ void load8_smem<BF16>(const uint8_t* base, int g, flo
 }
 
 template <>
-__device__ __forceinline__ void load8_smem<F32>(const uint8_t* base, int g, float x[8], float& vmax,
-                                                float& vmin) {
+__device__ __forceinline__ void load8_smem<F32>(const uint8_t* base, int g, float x[8], float& vmax) {
   const float4 a = *reinterpret_cast<const float4*>(base + 32 * g);
   const float4 b = *reinterpret_cast<const float4*>(base + 32 * g + 16);
   x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
   x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
   vmax = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
-  vmin = fminf(fminf(fminf(a.x, a.y), fminf(a.z, a.w)), fminf(fminf(b.x, b.y), fminf(b.z, b.w)));
 }
 
 // Up to 8 entries straight from global memory (any alignment); unused entries get kVoid.
 template <class DT>
-__device__ __forceinline__ void load_global(const void* row, int64_t v0, int n, float x[8], float& vmax,
-                                            float& vmin) {
+__device__ __forceinline__ void load_global(const void* row, int64_t v0, int n, float x[8], float& vmax) {
   vmax = kNegInf;
-  vmin = -kNegInf;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if (j < n) {
       x[j] = DT::load(row, v0 + j);
       vmax = fmaxf(vmax, x[j]);
-      vmin = fminf(vmin, x[j]);
     } else {
       x[j] = kVoid;
     }
   }
 }
 
-// Warp-level combine of two thread states (exact power-of-two rescaling).
-__device__ __forceinline__ void acc_merge(AccS& a, const AccS& b) {
-  const int nz = min(a.nz, b.nz);
-  const float fa = pow2i(nz - a.nz), fb = pow2i(nz - b.nz);
-  a.sz = a.sz * fa + b.sz * fb;
-  a.szd = a.szd * fa + b.szd * fb;
-  a.nz = nz;
-  const int nt = min(a.nt, b.nt);
-  a.st = a.st * pow2i(nt - a.nt) + b.st * pow2i(nt - b.nt);
-  a.nt = nt;
-  if (b.mt > a.mt || (b.mt == a.mt && b.bgrp < a.bgrp)) a.bgrp = b.bgrp;
-  a.mt = fmaxf(a.mt, b.mt);
-  a.dmax = fmaxf(a.dmax, b.dmax);
-}
-
-__device__ __forceinline__ AccS shfl_acc(const AccS& a, int off) {
-  AccS b;
-  b.sz = __shfl_xor_sync(0xffffffffu, a.sz, off);
-  b.szd = __shfl_xor_sync(0xffffffffu, a.szd, off);
-  b.nz = __shfl_xor_sync(0xffffffffu, a.nz, off);
-  b.st = __shfl_xor_sync(0xffffffffu, a.st, off);
-  b.nt = __shfl_xor_sync(0xffffffffu, a.nt, off);
-  b.mt = __shfl_xor_sync(0xffffffffu, a.mt, off);
-  b.dmax = __shfl_xor_sync(0xffffffffu, a.dmax, off);
-  b.bgrp = __shfl_xor_sync(0xffffffffu, a.bgrp, off);
-  return b;
+// Whole-warp combine: every lane first moves its sums to the warp's smallest
+// offset (an exact power-of-two scale), so only the three sums need shuffles; the
+// maxima and the argmax group use single-instruction warp reductions.  The xor
+// butterfly gives every lane the same sums.
+__device__ __forceinline__ AccS warp_reduce(const AccS& a) {
+  AccS r;
+  r.nz = __reduce_min_sync(0xffffffffu, a.nz);
+  r.nt = __reduce_min_sync(0xffffffffu, a.nt);
+  const float fz = pow2i(r.nz - a.nz), ft = pow2i(r.nt - a.nt);
+  float sz = a.sz * fz, szd = a.szd * fz, st = a.st * ft;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sz += __shfl_xor_sync(0xffffffffu, sz, off);
+    szd += __shfl_xor_sync(0xffffffffu, szd, off);
+    st += __shfl_xor_sync(0xffffffffu, st, off);
+  }
+  r.sz = sz; r.szd = szd; r.st = st;
+  r.mt = warp_max_f32(a.mt);
+  r.bgrp = static_cast<int>(__reduce_min_sync(0xffffffffu, static_cast<unsigned>(a.mt == r.mt ? a.bgrp : INT_MAX)));
+  r.dmax = warp_max_f32(a.dmax);
+  r.cmax = warp_max_f32(a.cmax);
+  return r;
 }
 
 // Fixed-order combine of partials; the power-of-two factors are exact.
@@ -343,7 +356,7 @@ __device__ __forceinline__ Unit map_unit(const RowPassParams& P, int u) {
 }  // namespace
 
 template <class DZ, class DT, bool kFast>
-__global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParams P) {
+__global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_kernel(const RowPassParams P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages];
   __shared__ uint64_t empty_bar[kStages];
@@ -352,12 +365,16 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
   __shared__ SlicePartial slots[2][kMaxCluster];
   __shared__ SliceCorr cslots[2][kMaxCluster];
   __shared__ SlicePartial warp_part[kConsumerWarps];
+  __shared__ float warp_cmax[kConsumerWarps];
   __shared__ float warp_corr[kConsumerWarps][2];
   __shared__ int warp_nclip[kConsumerWarps];
   __shared__ RowConsts rc;
   __shared__ int s_abort;
   __shared__ int s_unit_err;
 
+  // The acceptance scan / loss kernel that follows may be scheduled now; it waits
+  // for this grid's completion before reading what this grid writes.
+  asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -372,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
   // 128-byte aligned base for the bulk-copy ring (the launch adds 128 bytes of slack).
   uint8_t* ring =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-  float* codes = reinterpret_cast<float*>(ring + kStages * (kStageZ + kStageT));
+  // One screening code per consumer thread and slot: slot c < #chunks covers the
+  // thread's two groups of ring chunk c, later slots one directly loaded group each.
+  uint16_t* codes = reinterpret_cast<uint16_t*>(ring + kStages * (kStageZ + kStageT));
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -459,24 +478,26 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
           const uint8_t* stage = ring + st * (kStageZ + kStageT);
           const int gbase = (v_begin + e0) >> 3;  // row-global group index of the chunk's first group
           if (U.pair) {
+            float cm = kNegInf;
 #pragma unroll
             for (int k = 0; k < kGroupsPerThread; ++k) {
               const int g = tid + k * kConsumers;
               if (g < gcount) {
-                float z[8], t[8], vmz, vnz, vmt, vnt;
-                load8_smem<DZ>(stage, g, z, vmz, vnz);
-                load8_smem<DT>(stage + kStageZ, g, t, vmt, vnt);
-                codes[(e0 >> 3) + g] = vmz;
-                acc_pair(acc, z, t, vmz, vmt, vnt, gbase + g);
+                float z[8], t[8], vmz, vmt;
+                load8_smem<DZ>(stage, g, z, vmz);
+                load8_smem<DT>(stage + kStageZ, g, t, vmt);
+                acc_pair(acc, z, t, vmz, vmt, gbase + g);
+                cm = fmaxf(cm, vmz);
               }
             }
+            codes[(e0 / kChunk) * kConsumers + tid] = code_up(cm);
           } else {
 #pragma unroll
             for (int k = 0; k < kGroupsPerThread; ++k) {
               const int g = tid + k * kConsumers;
               if (g < gcount) {
-                float t[8], vmt, vnt;
-                load8_smem<DT>(stage + kStageZ, g, t, vmt, vnt);
+                float t[8], vmt;
+                load8_smem<DT>(stage + kStageZ, g, t, vmt);
                 acc_target(acc, vmt, gbase + g);
               }
             }
@@ -486,30 +507,33 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
         }
       }
       // Direct loads: the whole slice (unaligned rows) or the ragged tail group.
-      for (int g = (body >> 3) + tid; g < ngroups; g += kConsumers) {
+      // Group g is always handled by consumer thread g mod 256 (in the ring loop as
+      // here), so a thread's group maximum covers exactly the groups it re-reads.
+      const int nchunks = (body + kChunk - 1) / kChunk;
+      const int gd0 = (body >> 3) + ((tid - (body >> 3)) & (kConsumers - 1));  // this thread's first direct group
+      for (int g = gd0, slot = nchunks; g < ngroups; g += kConsumers, ++slot) {
         const int64_t v0 = v_begin + (static_cast<int64_t>(g) << 3);
         const int n = min(8, v_end - static_cast<int>(v0));
         const int grp = static_cast<int>(v0 >> 3);
-        float t[8], vmt, vnt;
-        load_global<DT>(trow, v0, n, t, vmt, vnt);
+        float t[8], vmt;
+        load_global<DT>(trow, v0, n, t, vmt);
         if (U.pair) {
-          float z[8], vmz, vnz;
-          load_global<DZ>(zrow, v0, n, z, vmz, vnz);
-          codes[g] = vmz;
-          acc_pair(acc, z, t, vmz, vmt, vnt, grp);
+          float z[8], vmz;
+          load_global<DZ>(zrow, v0, n, z, vmz);
+          acc_pair(acc, z, t, vmz, vmt, grp);
+          codes[slot * kConsumers + tid] = code_up(vmz);
         } else {
           acc_target(acc, vmt, grp);
         }
       }
 
       // ---- CTA reduction, then the exchange of slice partials ----
-      AccS as = acc_fold(acc);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc_merge(as, shfl_acc(as, off));
+      const AccS as = warp_reduce(acc_fold(acc));
       if (lane == 0) {
         SlicePartial& w = warp_part[warp];
         w.nz = as.nz; w.sz = as.sz; w.szd = as.szd;
         w.nt = as.nt; w.st = as.st; w.mt = as.mt; w.dmax = as.dmax; w.bgrp = as.bgrp; w.err = 0;
+        warp_cmax[warp] = as.cmax;
       }
       named_bar_sync(kConsumers);
 
@@ -544,6 +568,11 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
             const float th = rc.lse_z + logf(c / Rp);
             rc.theta = th - (1e-3f + 1e-5f * fabsf(th));
           }
+          float cm = kNegInf;
+          for (int w = 0; w < kConsumerWarps; ++w) cm = fmaxf(cm, warp_cmax[w]);
+          rc.scan = cm > rc.theta;
+        } else {
+          rc.scan = 0;
         }
       }
       named_bar_sync(kConsumers);
@@ -566,22 +595,40 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
       float corr = 0.f, sclip = 0.f;
       int nclip = 0;
       {
-        const float theta = U.bad ? INFINITY : rc.theta;
-        const TermConsts tc = make_term_consts(rc.lse_z, rc.lse_t);
-        const float c = P.clip_c;
-        for (int g = tid; g < ngroups; g += kConsumers) {
-          if (codes[g] > theta) {
-            const int v0 = v_begin + (g << 3);
-            const int n = min(8, v_end - v0);
-            for (int j = 0; j < n; ++j) {
-              const float zv = DZ::load(zrow, v0 + j);
-              const float tv = DT::load(trow, v0 + j);
-              float p, r, term;
-              entry_term(zv, tv, tc, p, r, term);  // the backward's evaluation, bit for bit
-              if (term > c) {
-                corr += term - c;
-                sclip = fmaf(p, r + 1.f, sclip);
-                ++nclip;
+        // A group can hold a clipped term only if its max z exceeds theta.  Each
+        // thread compares the largest group maximum it saw with theta (rarely
+        // above); only then does it walk its own codes and re-read, from global
+        // memory, the groups of the slots whose code is above theta.
+        const float theta = rc.theta;
+        if (!U.bad && rc.scan && acc.cmax > theta) {
+          const TermConsts tc = make_term_consts(rc.lse_z, rc.lse_t);
+          const float c = P.clip_c;
+          const int nchunks = (body + kChunk - 1) / kChunk;
+          const int gd0 = (body >> 3) + ((tid - (body >> 3)) & (kConsumers - 1));
+          const int nslots = nchunks + (ngroups > gd0 ? (ngroups - gd0 + kConsumers - 1) / kConsumers : 0);
+          for (int slot = 0; slot < nslots; ++slot) {
+            if (!(code_value(codes[slot * kConsumers + tid]) > theta)) continue;
+            for (int k = 0; k < (slot < nchunks ? kGroupsPerThread : 1); ++k) {
+              int g;
+              if (slot < nchunks) {
+                const int gl = tid + k * kConsumers;
+                if (gl >= (min(kChunk, body - slot * kChunk) >> 3)) continue;
+                g = slot * (kChunk / 8) + gl;
+              } else {
+                g = gd0 + (slot - nchunks) * kConsumers;
+              }
+              const int v0 = v_begin + (g << 3);
+              const int n = min(8, v_end - v0);
+              for (int j = 0; j < n; ++j) {
+                const float zv = DZ::load(zrow, v0 + j);
+                const float tv = DT::load(trow, v0 + j);
+                float p, r, term;
+                entry_term(zv, tv, tc, p, r, term);  // the backward's evaluation, bit for bit
+                if (term > c) {
+                  corr += term - c;
+                  sclip = fmaf(p, r + 1.f, sclip);
+                  ++nclip;
+                }
               }
             }
           }
@@ -654,10 +701,18 @@ __global__ void __launch_bounds__(kThreads, 2) rowpass_kernel(const RowPassParam
 // host side
 // ---------------------------------------------------------------------------
 
-int rowpass_cluster_size(int vocab) {
-  // about 40K entries per CTA; at most 8 CTAs (the portable cluster size)
-  int c = (vocab + 39999) / 40000;
-  return c < 1 ? 1 : (c > kMaxCluster ? kMaxCluster : c);
+#ifndef ADAFLASH_ROWPASS_SLICE_TARGET
+#define ADAFLASH_ROWPASS_SLICE_TARGET 160000
+#endif
+
+int rowpass_cluster_size(int vocab, int units, int num_sms) {
+  // At most ADAFLASH_ROWPASS_SLICE_TARGET entries per CTA, and enough CTAs in
+  // flight to fill the GPU (3 per SM) when there are few rows; at most 8 (the
+  // portable cluster size).
+  int c = (vocab + ADAFLASH_ROWPASS_SLICE_TARGET - 1) / ADAFLASH_ROWPASS_SLICE_TARGET;
+  if (c < 1) c = 1;
+  while (c < kMaxCluster && static_cast<long long>(units) * c < 3LL * num_sms) ++c;
+  return c > kMaxCluster ? kMaxCluster : c;
 }
 
 int rowpass_slice(int vocab, int cluster) {
@@ -681,7 +736,11 @@ int g_occ_n = 0;
 template <class DZ, class DT, bool kFast>
 static cudaError_t launch_one(const RowPassParams& p, cudaStream_t stream) {
   const size_t ring = static_cast<size_t>(kStages) * kChunk * (DZ::kBytes + DT::kBytes);
-  const size_t smem = 128 + ring + static_cast<size_t>((p.slice + 7) / 8) * sizeof(float);
+  // screening codes: per consumer thread one slot per ring chunk (+1 for a ragged
+  // tail group) on the bulk-copy path, one per group on the direct-load path
+  const int groups = (p.slice + 7) / 8;
+  const int slots = kFast ? ((p.slice + kChunk - 1) / kChunk + 1) : ((groups + kConsumers - 1) / kConsumers);
+  const size_t smem = 128 + ring + static_cast<size_t>(slots) * kConsumers * sizeof(uint16_t);
   auto kern = rowpass_kernel<DZ, DT, kFast>;
   const int units = (p.mode == kModeVerify) ? p.N_t : (p.N_d + p.R);
   if (units <= 0) return cudaSuccess;
