@@ -20,6 +20,8 @@ struct RowPassParams {
   int32_t mode;
   int32_t cluster;  // CTAs per row unit (1..8)
   int32_t slice;    // vocabulary entries per CTA (multiple of 8)
+  int32_t unit_begin, unit_end;  // units handled by this launch (set by launch_rowpass)
+  int32_t wait_prior;            // 1: complete only after the preceding launch has completed
   float clip_c;
   int32_t* target_argmax;
   float* kl_row;

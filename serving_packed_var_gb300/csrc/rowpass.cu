@@ -61,8 +61,12 @@ constexpr int kThreads = kConsumers + 32;  // + one producer warp
 #define ADAFLASH_ROWPASS_MINBLOCKS 3
 #endif
 constexpr int kStages = ADAFLASH_ROWPASS_STAGES;
-constexpr int kChunk = 4096;  // entries of each tensor per stage
+#ifndef ADAFLASH_ROWPASS_CHUNK
+#define ADAFLASH_ROWPASS_CHUNK 4096
+#endif
+constexpr int kChunk = ADAFLASH_ROWPASS_CHUNK;  // entries of each tensor per stage
 constexpr int kGroupsPerThread = kChunk / 8 / 256;  // 8-entry groups per consumer thread per chunk
+static_assert(kGroupsPerThread >= 1 && kChunk % 2048 == 0, "a chunk gives every consumer thread whole groups");
 constexpr int kMaxCluster = 8;
 constexpr int kNoOffset = 1 << 30;  // offset of an empty partial sum
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
   const int C = P.cluster;
   const int cid = static_cast<int>(blockIdx.x) / C;
   const int ncl = static_cast<int>(gridDim.x) / C;
-  const int num_units = (P.mode == kModeVerify) ? P.N_t : (P.N_d + P.R);
+  const int num_units = P.unit_end;
 
   constexpr int kStageZ = kChunk * DZ::kBytes;
   constexpr int kStageT = kChunk * DT::kBytes;
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
     // ---------------- producer warp: runs ahead across units ----------------
     if (kFast && lane == 0) {
       uint32_t cc = 0;
-      for (int u = cid; u < num_units && !*abort_flag; u += ncl) {
+      for (int u = P.unit_begin + cid; u < num_units && !*abort_flag; u += ncl) {
         const Unit U = map_unit(P, u);
         const int v_begin = static_cast<int>(rank) * P.slice;
         const int v_end = U.bad ? v_begin : min(P.V, v_begin + P.slice);
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
     // ---------------- consumer warps ----------------
     uint32_t cc = 0;
     int it = 0, pit = 0;
-    for (int u = cid; u < num_units; u += ncl, ++it) {
+    for (int u = P.unit_begin + cid; u < num_units; u += ncl, ++it) {
       const Unit U = map_unit(P, u);
       const int v_begin = static_cast<int>(rank) * P.slice;
       const int v_end = U.bad ? v_begin : min(P.V, v_begin + P.slice);
@@ -695,6 +699,9 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
 
   __syncthreads();
   cluster_sync_all();  // no CTA leaves while a peer may still address its shared memory
+  // A tail launch finishes only after the bulk launch before it, so whatever waits
+  // on this launch also sees every unit of the bulk launch.
+  if (P.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -733,54 +740,119 @@ OccEntry g_occ[64];
 int g_occ_n = 0;
 }  // namespace
 
+static int sm_count() {
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 152;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
 template <class DZ, class DT, bool kFast>
-static cudaError_t launch_one(const RowPassParams& p, cudaStream_t stream) {
+static size_t rowpass_smem(int slice) {
   const size_t ring = static_cast<size_t>(kStages) * kChunk * (DZ::kBytes + DT::kBytes);
   // screening codes: per consumer thread one slot per ring chunk (+1 for a ragged
   // tail group) on the bulk-copy path, one per group on the direct-load path
-  const int groups = (p.slice + 7) / 8;
-  const int slots = kFast ? ((p.slice + kChunk - 1) / kChunk + 1) : ((groups + kConsumers - 1) / kConsumers);
-  const size_t smem = 128 + ring + static_cast<size_t>(slots) * kConsumers * sizeof(uint16_t);
-  auto kern = rowpass_kernel<DZ, DT, kFast>;
-  const int units = (p.mode == kModeVerify) ? p.N_t : (p.N_d + p.R);
-  if (units <= 0) return cudaSuccess;
-  int device = 0;
-  cudaError_t e = cudaGetDevice(&device);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  const int groups = (slice + 7) / 8;
+  const int slots = kFast ? ((slice + kChunk - 1) / kChunk + 1) : ((groups + kConsumers - 1) / kConsumers);
+  return 128 + ring + static_cast<size_t>(slots) * kConsumers * sizeof(uint16_t);
+}
 
+// Co-resident clusters of this kernel at this cluster size (cached).
+template <class DZ, class DT, bool kFast>
+static int active_clusters(int cluster, size_t smem) {
+  auto kern = rowpass_kernel<DZ, DT, kFast>;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return 1;
+  // The query must see the shared-memory size the launch will use.
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 1;
+  }
+  for (int i = 0; i < g_occ_n; ++i)
+    if (g_occ[i].fn == reinterpret_cast<const void*>(kern) && g_occ[i].smem == smem &&
+        g_occ[i].cluster == cluster && g_occ[i].device == device)
+      return g_occ[i].clusters;
   cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-
-  int clusters = -1;
-  for (int i = 0; i < g_occ_n; ++i)
-    if (g_occ[i].fn == reinterpret_cast<const void*>(kern) && g_occ[i].smem == smem &&
-        g_occ[i].cluster == p.cluster && g_occ[i].device == device)
-      clusters = g_occ[i].clusters;
-  if (clusters < 0) {
-    cfg.gridDim = dim3(static_cast<unsigned>(p.cluster), 1, 1);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
-      (void)cudaGetLastError();
-      n = 1;
-    }
-    clusters = n;
-    if (g_occ_n < 64) g_occ[g_occ_n++] = OccEntry{reinterpret_cast<const void*>(kern), smem, p.cluster, device, n};
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    n = sm_count() / cluster;  // one CTA per SM: always resident
+    if (n < 1) n = 1;
   }
-  // One persistent cluster per co-resident slot (clusters never wait on one another).
+  if (g_occ_n < 64) g_occ[g_occ_n++] = OccEntry{reinterpret_cast<const void*>(kern), smem, cluster, device, n};
+  return n;
+}
+
+// One launch over units [p.unit_begin, p.unit_end), persistent clusters.
+template <class DZ, class DT, bool kFast>
+static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaStream_t stream) {
+  const size_t smem = rowpass_smem<DZ, DT, kFast>(p.slice);
+  auto kern = rowpass_kernel<DZ, DT, kFast>;
+  const int units = p.unit_end - p.unit_begin;
+  if (units <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int clusters = active_clusters<DZ, DT, kFast>(p.cluster, smem);
+  cudaLaunchConfig_t cfg = {};
   const int grid_clusters = units < clusters ? units : clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters) * static_cast<unsigned>(p.cluster), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = programmatic ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Whole waves of units run at the requested cluster size; when the units do not
+// fill the last wave, the remainder (the last rows, and the cheap target-only
+// rows) runs as a second launch with larger clusters, so its rows are split
+// over more CTAs instead of leaving a few CTAs to finish whole rows alone.  The
+// second launch starts as CTAs of the first retire (programmatic launch) and
+// completes only after the first.
+template <class DZ, class DT, bool kFast>
+static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
+  const int units = (p0.mode == kModeVerify) ? p0.N_t : (p0.N_d + p0.R);
+  if (units <= 0) return cudaSuccess;
+  RowPassParams p = p0;
+  p.unit_begin = 0;
+  p.unit_end = units;
+  p.wait_prior = 0;
+  const int clusters = active_clusters<DZ, DT, kFast>(p.cluster, rowpass_smem<DZ, DT, kFast>(p.slice));
+  const int split = (units / clusters) * clusters;
+  if (units <= clusters || split == units || p.cluster >= kMaxCluster) return launch_range<DZ, DT, kFast>(p, false, stream);
+  RowPassParams tail = p;
+  p.unit_end = split;
+  cudaError_t e = launch_range<DZ, DT, kFast>(p, false, stream);
+  if (e != cudaSuccess) return e;
+  tail.unit_begin = split;
+  tail.unit_end = units;
+  tail.wait_prior = 1;
+  tail.cluster = rowpass_cluster_size(p.V, units - split, sm_count());
+  if (tail.cluster < p.cluster) tail.cluster = p.cluster;
+  tail.slice = rowpass_slice(p.V, tail.cluster);
+  return launch_range<DZ, DT, kFast>(tail, true, stream);
 }
 
 cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s) {
