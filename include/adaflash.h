@@ -144,6 +144,11 @@ adaflash_status adaflash_opd_loss_bwd(
     float* grad_draft, int64_t ld_g,
     uint32_t* d_status, void* stream);
 
+/* Number of kernel launches this library has enqueued in this process so far
+ * (all entry points, all devices).  For instrumentation: the difference over a
+ * region of calls counts the kernels that region launched. */
+uint64_t adaflash_kernel_launches(void);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* adaflash_status_string(adaflash_status status);
 

@@ -32,6 +32,7 @@ __all__ = [
     "adaflash_opd_loss_bwd",
     "adaflash_selftest_bounded_wait",
     "adaflash_status_string",
+    "adaflash_kernel_launches",
     "status_bits",
 ]
 
@@ -44,6 +45,11 @@ class AdaflashError(RuntimeError):
 
 def adaflash_status_string(code: int) -> str:
     return _native.status_string(code)
+
+
+def adaflash_kernel_launches() -> int:
+    """Kernel launches this library has enqueued in this process so far."""
+    return int(_native.lib().adaflash_kernel_launches())
 
 
 def status_bits(word: int):

@@ -39,6 +39,7 @@ SIGNATURES = {
                               _vp, _vp, _vp, _f32, _vp, _i64, _vp, _vp],
     "adaflash_selftest_bounded_wait": [_vp, _i32, _vp],
     "adaflash_status_string": [_i32],
+    "adaflash_kernel_launches": [],
 }
 
 _lib = None
@@ -61,7 +62,8 @@ def lib() -> ctypes.CDLL:
     for name, args in SIGNATURES.items():
         fn = getattr(L, name)
         fn.argtypes = args
-        fn.restype = ctypes.c_char_p if name == "adaflash_status_string" else ctypes.c_int
+        fn.restype = {"adaflash_status_string": ctypes.c_char_p,
+                      "adaflash_kernel_launches": ctypes.c_uint64}.get(name, ctypes.c_int)
     _lib = L
     return L
 

@@ -3,6 +3,7 @@
 // Host-side argument validation happens before any CUDA call, so malformed calls
 // return at once and enqueue nothing.  Every accepted call enqueues its kernels on
 // the caller's stream and returns without synchronising.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -84,7 +85,14 @@ int num_sms() {
 
 }  // namespace
 
+namespace adaflash {
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace adaflash
+
 extern "C" {
+
+uint64_t adaflash_kernel_launches(void) { return adaflash::g_launches.load(std::memory_order_relaxed); }
 
 const char* adaflash_status_string(adaflash_status s) {
   switch (s) {

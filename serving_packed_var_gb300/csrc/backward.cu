@@ -139,6 +139,7 @@ template <class DZ, class DT, bool kFast>
 static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t s) {
   const long long blocks = static_cast<long long>(p.N_d) * p.chunks_per_row;
   if (blocks <= 0) return cudaSuccess;
+  count_launch();
   bwd_kernel<DZ, DT, kFast><<<static_cast<unsigned>(blocks), kBwdThreads, 0, s>>>(p);
   return cudaGetLastError();
 }

@@ -102,6 +102,7 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, finalize_kernel, p);
 }
 
@@ -121,6 +122,7 @@ __global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns) {
 }
 
 cudaError_t launch_selftest_wait(uint32_t* status, int32_t limit_us, cudaStream_t s) {
+  count_launch();
   selftest_wait_kernel<<<1, 32, 0, s>>>(status, static_cast<uint64_t>(limit_us) * 1000ull);
   return cudaGetLastError();
 }

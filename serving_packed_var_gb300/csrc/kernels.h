@@ -62,6 +62,9 @@ struct BwdParams {
   uint32_t* status;
 };
 
+// Launch counter behind adaflash_kernel_launches (incremented once per launch).
+void count_launch();
+
 // dtype codes match adaflash_dtype (0 = fp32, 1 = bf16)
 cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);

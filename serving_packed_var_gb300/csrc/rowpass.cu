@@ -10,7 +10,7 @@
 //                     ring of shared-memory stages (mbarrier-signalled), running
 //                     ahead across unit boundaries;
 //   8 consumer warps: per 8-entry group, an online log-sum-exp of z and of t,
-//                     sum_v e^{z_v}(z_v - t_v), a bound
+//                     sum_v e^{z_v}(z_v - t_v) (packed f32x2 arithmetic), a bound
 //                     on max_v (z_v - t_v), the lowest-index argmax of t, and the
 //                     largest group maximum of z each thread sees.
 //
@@ -192,24 +192,35 @@ __device__ __forceinline__ void acc_pair(Acc& a, const float z[8], const float t
   a.mt = fmaxf(a.mt, vmt);
   a.bgrp = nb ? grp : a.bgrp;
   a.cmax = fmaxf(a.cmax, vmz);
-  float dm0 = a.dmax, dm1 = kNegInf;
+  {
+    // Two entries per instruction on the FMA pipe (f32x2): even/odd entries are the
+    // two lanes of each packed register, matching the two accumulators.
+    const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
+    const uint64_t nz2 = f2_pack(a.nzf, a.nzf), nt2 = f2_pack(a.ntf, a.ntf);
+    uint64_t SZ = f2_pack(a.sz0, a.sz1), ST = f2_pack(a.st0, a.st1), SD = f2_pack(a.szd0, a.szd1);
+    float dm0 = a.dmax, dm1 = kNegInf;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float ez0 = ex2(fmaf(z[2 * q], kLog2e, a.nzf));
-    const float ez1 = ex2(fmaf(z[2 * q + 1], kLog2e, a.nzf));
-    const float et0 = ex2(fmaf(t[2 * q], kLog2e, a.ntf));
-    const float et1 = ex2(fmaf(t[2 * q + 1], kLog2e, a.ntf));
-    a.sz0 += ez0;
-    a.sz1 += ez1;
-    a.st0 += et0;
-    a.st1 += et1;
-    const float d0 = z[2 * q] - t[2 * q], d1 = z[2 * q + 1] - t[2 * q + 1];
-    a.szd0 = fmaf(ez0, d0, a.szd0);
-    a.szd1 = fmaf(ez1, d1, a.szd1);
-    dm0 = fmaxf(dm0, d0);
-    dm1 = fmaxf(dm1, d1);
+    for (int q = 0; q < 4; ++q) {
+      const uint64_t Z = f2_pack(z[2 * q], z[2 * q + 1]);
+      const uint64_t T = f2_pack(t[2 * q], t[2 * q + 1]);
+      float az0, az1, at0, at1;
+      f2_unpack(f2_fma(Z, l2e2, nz2), az0, az1);
+      f2_unpack(f2_fma(T, l2e2, nt2), at0, at1);
+      const uint64_t EZ = f2_pack(ex2(az0), ex2(az1));
+      SZ = f2_add(SZ, EZ);
+      ST = f2_add(ST, f2_pack(ex2(at0), ex2(at1)));
+      const uint64_t D = f2_sub(Z, T);
+      SD = f2_fma(EZ, D, SD);
+      float d0, d1;
+      f2_unpack(D, d0, d1);
+      dm0 = fmaxf(dm0, d0);
+      dm1 = fmaxf(dm1, d1);
+    }
+    f2_unpack(SZ, a.sz0, a.sz1);
+    f2_unpack(ST, a.st0, a.st1);
+    f2_unpack(SD, a.szd0, a.szd1);
+    a.dmax = fmaxf(dm0, dm1);
   }
-  a.dmax = fmaxf(dm0, dm1);
 }
 
 // Target-only group: argmax only.
@@ -822,6 +833,7 @@ static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaS
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = programmatic ? 2 : 1;
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
