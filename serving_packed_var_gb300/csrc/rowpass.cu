@@ -75,6 +75,7 @@ struct __align__(16) SlicePartial {
   float sz, szd, st;  // sums scaled by 2^{nz}, 2^{nz}, 2^{nt}
   int nz, nt;         // integer base-2 exponent offsets
   float mt, dmax;     // max of t, bound on max of z - t
+  float cmax;         // largest group maximum of z in the slice
   int bgrp;           // first group holding the max of t
   int err;
 };
@@ -91,7 +92,8 @@ struct RowConsts {
   int argmax;
   int err;
   int stop;  // every consumer thread leaves the unit loop together when set
-  int scan;  // some thread of this CTA saw a group maximum of z above the threshold
+  int scan;      // some thread of this CTA saw a group maximum of z above the threshold
+  int any_scan;  // some CTA of the cluster did (the corrections are exchanged)
 };
 
 // Per-thread running state.  Sums are kept relative to integer base-2 exponent
@@ -307,8 +309,9 @@ __device__ __forceinline__ AccS warp_reduce(const AccS& a) {
 // Fixed-order combine of partials; the power-of-two factors are exact.
 __device__ void combine_partials(const SlicePartial* parts, int n, SlicePartial& out) {
   int nz = kNoOffset, nt = kNoOffset, bgrp = INT_MAX, err = 0;
-  float mt = kNegInf, dmax = kNegInf;
+  float mt = kNegInf, dmax = kNegInf, cmax = kNegInf;
   for (int i = 0; i < n; ++i) {
+    cmax = fmaxf(cmax, parts[i].cmax);
     nz = min(nz, parts[i].nz);
     nt = min(nt, parts[i].nt);
     dmax = fmaxf(dmax, parts[i].dmax);
@@ -323,7 +326,7 @@ __device__ void combine_partials(const SlicePartial* parts, int n, SlicePartial&
     szd = fmaf(parts[i].szd, f, szd);
     st = fmaf(parts[i].st, pow2i(nt - parts[i].nt), st);
   }
-  out.nz = nz; out.nt = nt; out.mt = mt; out.dmax = dmax; out.bgrp = bgrp; out.err = err;
+  out.nz = nz; out.nt = nt; out.mt = mt; out.dmax = dmax; out.cmax = cmax; out.bgrp = bgrp; out.err = err;
   out.sz = sz; out.szd = szd; out.st = st;
 }
 
@@ -380,7 +383,6 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
   __shared__ SlicePartial slots[2][kMaxCluster];
   __shared__ SliceCorr cslots[2][kMaxCluster];
   __shared__ SlicePartial warp_part[kConsumerWarps];
-  __shared__ float warp_cmax[kConsumerWarps];
   __shared__ float warp_corr[kConsumerWarps][2];
   __shared__ int warp_nclip[kConsumerWarps];
   __shared__ RowConsts rc;
@@ -548,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
         SlicePartial& w = warp_part[warp];
         w.nz = as.nz; w.sz = as.sz; w.szd = as.szd;
         w.nt = as.nt; w.st = as.st; w.mt = as.mt; w.dmax = as.dmax; w.bgrp = as.bgrp; w.err = 0;
-        warp_cmax[warp] = as.cmax;
+        w.cmax = as.cmax;
       }
       named_bar_sync(kConsumers);
 
@@ -558,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
         combine_partials(warp_part, kConsumerWarps, mine);
         mine.err = s_unit_err;
         s_unit_err = 0;
+        const float own_cmax = mine.cmax;
         for (int r = 0; r < C; ++r) *map_to_rank(&slots[buf][rank], static_cast<uint32_t>(r)) = mine;
         for (int r = 0; r < C; ++r) mbar_arrive_remote(&part_bar[buf], static_cast<uint32_t>(r));
         int werr = 0;
@@ -583,11 +586,14 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
             const float th = rc.lse_z + logf(c / Rp);
             rc.theta = th - (1e-3f + 1e-5f * fabsf(th));
           }
-          float cm = kNegInf;
-          for (int w = 0; w < kConsumerWarps; ++w) cm = fmaxf(cm, warp_cmax[w]);
-          rc.scan = cm > rc.theta;
+          rc.scan = own_cmax > rc.theta;
+          // The same decision in every CTA of the cluster: with no group maximum
+          // above theta anywhere in the row, no term can clip and the exchange of
+          // corrections is skipped.
+          rc.any_scan = all.cmax > rc.theta;
         } else {
           rc.scan = 0;
+          rc.any_scan = 0;
         }
       }
       named_bar_sync(kConsumers);
@@ -602,6 +608,32 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
             if (rc.err) flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
           }
         }
+        if (stop) break;
+        continue;
+      }
+
+      // Rank 0 writes the row's outputs from the row constants and the summed corrections.
+      auto finish_row = [&](float corr_all, float sclip_all, int nclip_all, int err_all) {
+        if (U.bad) {
+          flag_status(P.status, ADAFLASH_ERR_BAD_OFFSETS);
+        } else if (rc.argmax < 0 || rc.argmax >= P.V) {
+          // only after an aborted unit (no group was reduced): nothing valid to write
+          flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
+        } else {
+          const int a = rc.argmax;
+          const int64_t d = U.d;
+          P.kl_row[d] = rc.kl_unclip - corr_all;
+          P.ce_row[d] = rc.lse_z - DZ::load(zrow, a);
+          P.row_stats[4 * d + 0] = rc.lse_z;
+          P.row_stats[4 * d + 1] = rc.lse_t;
+          P.row_stats[4 * d + 2] = (rc.kl_unclip + 1.f) - sclip_all;
+          P.row_stats[4 * d + 3] = static_cast<float>(nclip_all);
+          P.target_argmax[U.s] = a;
+          if (err_all) flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
+        }
+      };
+      if (!rc.any_scan) {
+        if (rank == 0 && tid == 0) finish_row(0.f, 0.f, 0, rc.err);
         if (stop) break;
         continue;
       }
@@ -675,31 +707,15 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
         if (rank == 0) {
           const bool ok = mbar_wait_cluster_bounded(&corr_bar[cbuf], (pit >> 1) & 1);
           if (!ok) *abort_flag = 1;
-          if (U.bad) {
-            flag_status(P.status, ADAFLASH_ERR_BAD_OFFSETS);
-          } else if (rc.argmax < 0 || rc.argmax >= P.V) {
-            // only after an aborted unit (no group was reduced): nothing valid to write
-            flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
-          } else {
-            float corr_all = 0.f, sclip_all = 0.f;
-            int nclip_all = 0, err_all = rc.err | (ok ? 0 : 1);
-            for (int r = 0; r < C; ++r) {
-              corr_all += cslots[cbuf][r].corr;
-              sclip_all += cslots[cbuf][r].sclip;
-              nclip_all += cslots[cbuf][r].nclip;
-              err_all |= cslots[cbuf][r].err;
-            }
-            const int a = rc.argmax;
-            const int64_t d = U.d;
-            P.kl_row[d] = rc.kl_unclip - corr_all;
-            P.ce_row[d] = rc.lse_z - DZ::load(zrow, a);
-            P.row_stats[4 * d + 0] = rc.lse_z;
-            P.row_stats[4 * d + 1] = rc.lse_t;
-            P.row_stats[4 * d + 2] = (rc.kl_unclip + 1.f) - sclip_all;
-            P.row_stats[4 * d + 3] = static_cast<float>(nclip_all);
-            P.target_argmax[U.s] = a;
-            if (err_all) flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
+          float corr_all = 0.f, sclip_all = 0.f;
+          int nclip_all = 0, err_all = rc.err | (ok ? 0 : 1);
+          for (int r = 0; r < C; ++r) {
+            corr_all += cslots[cbuf][r].corr;
+            sclip_all += cslots[cbuf][r].sclip;
+            nclip_all += cslots[cbuf][r].nclip;
+            err_all |= cslots[cbuf][r].err;
           }
+          finish_row(corr_all, sclip_all, nclip_all, err_all);
         }
       }
       ++pit;
