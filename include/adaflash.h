@@ -126,7 +126,7 @@ adaflash_status adaflash_opd_loss_fwd(
  *
  * Training updates the serving draft model from each round's verification
  * (AdaFlash article, "On-Policy Distillation (OPD) for Domain Adaptation"); the
- * target is a constant ("the target model never changes").  With g_r =
+ * target is a constant (it is never updated).  With g_r =
  * grad_row[r] (or grad_scale when grad_row is NULL), m_v = [p_v r_v <= clip_c]
  * and a the target argmax:
  *   grad_draft[r, v] = g_r * ( p_v (m_v (r_v + 1) - S) + ce_weight (p_v - [v == a]) )
@@ -142,6 +142,47 @@ adaflash_status adaflash_opd_loss_bwd(
     const int32_t* target_argmax, const float* row_stats,
     const float* grad_row, float grad_scale,
     float* grad_draft, int64_t ld_g,
+    uint32_t* d_status, void* stream);
+
+/*
+ * adaflash_verify_sampled -- temperature-sampled verification of packed draft blocks.
+ *
+ * The target verifies the drafted tokens in parallel (AdaFlash article, opening
+ * section) at the sampling temperature, a tunable of the method (page "AdaFlash
+ * Adaptive Speculative Decoding", section "Implementation Steps").  The rule is
+ * speculative sampling, with p = softmax(z / T) of a draft row and q = softmax(t / T)
+ * of its paired target row:
+ *   - draft token x_j is accepted when u_accept[d] * p(x_j) < q(x_j), d its draft row;
+ *     accept_len[i] = L_i is the number of tokens before the first rejection;
+ *   - L_i < k_i: the emitted token is drawn from max(0, q - p) at position L_i
+ *     (from q when that is all zero); L_i = k_i: from q at the bonus row;
+ *   - a draw from weights pi with w = u_sample[i] is the smallest v whose prefix sum
+ *     sum_{u<=v} pi_u exceeds w * sum_u pi_u (the inverse CDF in vocabulary order).
+ * The uniforms are inputs, so the caller owns the random stream.  w is clamped to
+ * [0, 1] (NaN -> 0); a NaN u rejects.  Logits are finite or -inf.
+ *
+ *   draft_logits   [N_d, ld_d] of d_dtype           in
+ *   target_logits  [N_t, ld_t] of t_dtype           in
+ *   draft_tokens   int32 [N_d]                      in
+ *   draft_offsets  int32 [R+1]                      in
+ *   temperature    T > 0 with 1/T finite            in
+ *   u_accept       float [N_d]                      in: accept uniforms in [0, 1)
+ *   u_sample       float [R]                        in: draw uniforms in [0, 1)
+ *   row_lse        float [N_d + N_t]                out: logsumexp(x / T) of each draft row,
+ *                                                        then of each target row
+ *   accept_len     int32 [R]                        out: L_i
+ *   next_token     int32 [R]                        out: the emitted token
+ *   accept_rate    float [R]                        out: L_i / k_i rounded once to float32
+ * A request with malformed offsets gets accept_len = next_token = -1, accept_rate = -1.
+ * A draft token outside [0, vocab) is rejected and sets ADAFLASH_ERR_BAD_TOKEN.
+ */
+adaflash_status adaflash_verify_sampled(
+    const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
+    const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
+    const int32_t* draft_tokens, const int32_t* draft_offsets,
+    int32_t num_requests, int32_t num_draft_rows, int32_t vocab,
+    float temperature, const float* u_accept, const float* u_sample,
+    float* row_lse, int32_t* accept_len, int32_t* next_token, float* accept_rate,
     uint32_t* d_status, void* stream);
 
 /* Number of kernel launches this library has enqueued in this process so far

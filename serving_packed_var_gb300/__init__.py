@@ -30,6 +30,7 @@ __all__ = [
     "adaflash_verify_packed",
     "adaflash_opd_loss_fwd",
     "adaflash_opd_loss_bwd",
+    "adaflash_verify_sampled",
     "adaflash_selftest_bounded_wait",
     "adaflash_status_string",
     "adaflash_kernel_launches",
@@ -166,6 +167,35 @@ def adaflash_opd_loss_bwd(draft_logits, target_logits, draft_offsets, target_arg
         _ptr(grad_row), float(grad_scale), gp, ldg, _ptr(status), _stream(stream))
     _check(code, "adaflash_opd_loss_bwd")
     return g
+
+
+def adaflash_verify_sampled(draft_logits, target_logits, draft_tokens, draft_offsets, temperature, u_accept,
+                            u_sample, vocab=None, out=None, status=None, stream=None):
+    """Temperature-sampled verification with caller-supplied uniforms.
+
+    Returns dict(row_lse, accept_len, next_token, accept_rate).
+    """
+    zp, ldz = _rows(draft_logits, "draft_logits")
+    tp, ldt = _rows(target_logits, "target_logits")
+    dev = draft_logits.device
+    R = draft_offsets.numel() - 1
+    Nd = draft_tokens.numel()
+    V = draft_logits.shape[1] if vocab is None else vocab
+    for name, u, n in (("u_accept", u_accept, Nd), ("u_sample", u_sample, R)):
+        if u.dtype != torch.float32 or u.numel() != n or not u.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 tensor of {n} entries")
+    o = dict(out or {})
+    o.setdefault("row_lse", _f32(2 * Nd + R, dev))
+    o.setdefault("accept_len", _i32(R, dev))
+    o.setdefault("next_token", _i32(R, dev))
+    o.setdefault("accept_rate", _f32(R, dev))
+    code = _native.lib().adaflash_verify_sampled(
+        zp, _dtype_code(draft_logits), ldz, tp, _dtype_code(target_logits), ldt,
+        draft_tokens.data_ptr(), draft_offsets.data_ptr(), R, Nd, V, float(temperature),
+        u_accept.data_ptr(), u_sample.data_ptr(), o["row_lse"].data_ptr(), o["accept_len"].data_ptr(),
+        o["next_token"].data_ptr(), o["accept_rate"].data_ptr(), _ptr(status), _stream(stream))
+    _check(code, "adaflash_verify_sampled")
+    return o
 
 
 def adaflash_selftest_bounded_wait(status, limit_us=1000, stream=None):

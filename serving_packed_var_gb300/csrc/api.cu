@@ -264,6 +264,51 @@ adaflash_status adaflash_opd_loss_bwd(const void* draft_logits, adaflash_dtype d
   return ADAFLASH_OK;
 }
 
+adaflash_status adaflash_verify_sampled(const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
+                                        const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
+                                        const int32_t* draft_tokens, const int32_t* draft_offsets,
+                                        int32_t num_requests, int32_t num_draft_rows, int32_t vocab,
+                                        float temperature, const float* u_accept, const float* u_sample,
+                                        float* row_lse, int32_t* accept_len, int32_t* next_token,
+                                        float* accept_rate, uint32_t* d_status, void* stream) {
+  ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  ADAFLASH_TRY(check_logits(draft_logits, d_dtype, ld_d, vocab));
+  ADAFLASH_TRY(check_logits(target_logits, t_dtype, ld_t, vocab));
+  if (!int_ptr_ok(draft_tokens) || !int_ptr_ok(draft_offsets) || !int_ptr_ok(u_accept) ||
+      !int_ptr_ok(u_sample) || !int_ptr_ok(row_lse) || !int_ptr_ok(accept_len) || !int_ptr_ok(next_token) ||
+      !int_ptr_ok(accept_rate))
+    return ADAFLASH_ERR_INVALID_ARG;
+  if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature) || !std::isfinite(1.0f / temperature))
+    return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_device());
+  if (num_requests == 0) return ADAFLASH_OK;
+
+  SampledParams p = {};
+  p.z = draft_logits;
+  p.t = target_logits;
+  p.ld_z = ld_d;
+  p.ld_t = ld_t;
+  p.z_vec = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) ? 1 : 0;
+  p.t_vec = rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)) ? 1 : 0;
+  p.doff = draft_offsets;
+  p.R = num_requests;
+  p.N_d = num_draft_rows;
+  p.N_t = num_draft_rows + num_requests;
+  p.V = vocab;
+  p.inv_t = 1.0f / temperature;
+  p.tokens = draft_tokens;
+  p.u_accept = u_accept;
+  p.u_sample = u_sample;
+  p.row_lse = row_lse;
+  p.accept_len = accept_len;
+  p.next_token = next_token;
+  p.accept_rate = accept_rate;
+  p.status = d_status;
+  ADAFLASH_CUDA(launch_sampled(p, d_dtype, t_dtype, static_cast<cudaStream_t>(stream)));
+  return ADAFLASH_OK;
+}
+
 adaflash_status adaflash_selftest_bounded_wait(uint32_t* d_status, int32_t limit_us, void* stream) {
   if (!int_ptr_ok(d_status) || limit_us < 1 || limit_us > 1000000) return ADAFLASH_ERR_INVALID_ARG;
   ADAFLASH_TRY(check_device());

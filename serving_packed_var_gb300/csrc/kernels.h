@@ -62,6 +62,24 @@ struct BwdParams {
   uint32_t* status;
 };
 
+struct SampledParams {
+  const void* z;  // draft logits [N_d, ld_z]
+  const void* t;  // target logits [N_t, ld_t]
+  int64_t ld_z, ld_t;
+  int32_t z_vec, t_vec;  // 1: every row starts on a 16-byte boundary
+  const int32_t* doff;
+  int32_t R, N_d, N_t, V;
+  float inv_t;  // 1 / temperature
+  const int32_t* tokens;
+  const float* u_accept;  // [N_d]
+  const float* u_sample;  // [R]
+  float* row_lse;         // [N_d + N_t]: draft rows, then target rows
+  int32_t* accept_len;
+  int32_t* next_token;
+  float* accept_rate;
+  uint32_t* status;
+};
+
 // Launch counter behind adaflash_kernel_launches (incremented once per launch).
 void count_launch();
 
@@ -69,6 +87,7 @@ void count_launch();
 cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
+cudaError_t launch_sampled(const SampledParams& p, int z_dtype, int t_dtype, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t* status, int32_t limit_us, cudaStream_t s);
 
 // Geometry chosen for a vocabulary size (shared by host validation and launches).

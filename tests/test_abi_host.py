@@ -92,6 +92,30 @@ def test_bwd_rejects(lib, kw):
     assert _bwd(lib, **kw) == INVALID
 
 
+def _sampled(lib, **kw):
+    a = dict(z=FAKE, zd=1, ldz=1024, t=FAKE, td=1, ldt=1024, tok=FAKE, doff=FAKE, R=4, Nd=29, V=1024, T=1.0,
+             ua=FAKE, us=FAKE, lse=FAKE, acc=FAKE, nxt=FAKE, rate=FAKE, status=None)
+    a.update(kw)
+    return lib.adaflash_verify_sampled(a["z"], a["zd"], a["ldz"], a["t"], a["td"], a["ldt"], a["tok"], a["doff"],
+                                       a["R"], a["Nd"], a["V"], a["T"], a["ua"], a["us"], a["lse"], a["acc"],
+                                       a["nxt"], a["rate"], a["status"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(z=None), dict(t=None), dict(tok=None), dict(doff=None), dict(ua=None), dict(us=None), dict(lse=None),
+    dict(acc=None), dict(nxt=None), dict(rate=None), dict(ua=FAKE + 2), dict(lse=FAKE + 1), dict(T=0.0),
+    dict(T=-1.0), dict(T=float("nan")), dict(T=float("inf")), dict(T=1e-45), dict(ldz=100), dict(td=5),
+    dict(Nd=3), dict(status=FAKE + 3),
+])
+def test_sampled_rejects(lib, kw):
+    assert _sampled(lib, **kw) == INVALID
+
+
+def test_sampled_vocab_too_large(lib):
+    V = _native.ADAFLASH_MAX_VOCAB + 1
+    assert _sampled(lib, V=V, ldz=V, ldt=V) == UNSUPPORTED
+
+
 def test_selftest_rejects_bad_limit(lib):
     assert lib.adaflash_selftest_bounded_wait(FAKE, 0, None) == INVALID
     assert lib.adaflash_selftest_bounded_wait(None, 10, None) == INVALID
