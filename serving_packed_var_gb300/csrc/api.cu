@@ -289,8 +289,6 @@ adaflash_status adaflash_verify_sampled(const void* draft_logits, adaflash_dtype
   p.t = target_logits;
   p.ld_z = ld_d;
   p.ld_t = ld_t;
-  p.z_vec = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) ? 1 : 0;
-  p.t_vec = rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)) ? 1 : 0;
   p.doff = draft_offsets;
   p.R = num_requests;
   p.N_d = num_draft_rows;
@@ -305,7 +303,7 @@ adaflash_status adaflash_verify_sampled(const void* draft_logits, adaflash_dtype
   p.next_token = next_token;
   p.accept_rate = accept_rate;
   p.status = d_status;
-  ADAFLASH_CUDA(launch_sampled(p, d_dtype, t_dtype, static_cast<cudaStream_t>(stream)));
+  ADAFLASH_CUDA(launch_sampled(p, d_dtype, t_dtype, num_sms(), static_cast<cudaStream_t>(stream)));
   return ADAFLASH_OK;
 }
 

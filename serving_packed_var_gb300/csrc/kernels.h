@@ -66,7 +66,6 @@ struct SampledParams {
   const void* z;  // draft logits [N_d, ld_z]
   const void* t;  // target logits [N_t, ld_t]
   int64_t ld_z, ld_t;
-  int32_t z_vec, t_vec;  // 1: every row starts on a 16-byte boundary
   const int32_t* doff;
   int32_t R, N_d, N_t, V;
   float inv_t;  // 1 / temperature
@@ -87,7 +86,7 @@ void count_launch();
 cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
-cudaError_t launch_sampled(const SampledParams& p, int z_dtype, int t_dtype, cudaStream_t s);
+cudaError_t launch_sampled(const SampledParams& p, int z_dtype, int t_dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t* status, int32_t limit_us, cudaStream_t s);
 
 // Geometry chosen for a vocabulary size (shared by host validation and launches).

@@ -11,11 +11,15 @@
 //   that is all zero); when all are accepted it is drawn from q at the bonus row;
 //   a draw with uniform w is the smallest v whose prefix sum exceeds w * total.
 //
-// S1 computes log-sum-exp(x / T) of every draft row and every target row (one
-// read of each logit, 128-bit loads where rows are 16-byte aligned), S2 applies the
-// accept rule (one warp per request, k <= 16 lanes), S3 draws the emitted token
-// (one CTA per request: fixed-order per-thread sums over contiguous chunks, a block
-// scan, then one thread walks the chunk that holds the threshold).
+// Two kernels:
+//   S1 computes log-sum-exp(x / T) of every draft row and every target row, one
+//      read of each logit.  A cluster of C CTAs shares a row (each a slice of its
+//      8-entry groups); the partial (max, sum) pairs meet in CTA 0's shared memory.
+//   S2 is one cluster of 8 CTAs per request, launched as a programmatic dependent
+//      of S1: warp 0 applies the accept rule (k <= 16 lanes), then the cluster
+//      draws the emitted token (fixed-order sums over one contiguous segment per
+//      warp, CTA sums exchanged through distributed shared memory, and the warp
+//      whose segment holds the threshold walks it).
 #include <climits>
 #include <cmath>
 
@@ -26,11 +30,30 @@ namespace adaflash {
 
 namespace {
 
-constexpr int kLseThreads = 256;
-constexpr int kDrawThreads = 1024;
+#ifndef ADAFLASH_LSE_THREADS
+#define ADAFLASH_LSE_THREADS 256
+#endif
+#ifndef ADAFLASH_LSE_UNROLL
+#define ADAFLASH_LSE_UNROLL 8
+#endif
+#ifndef ADAFLASH_LSE_MINBLOCKS
+#define ADAFLASH_LSE_MINBLOCKS 4  // resident S1 CTAs per SM the register budget must allow
+#endif
+#ifndef ADAFLASH_LSE_ROWS_PER_SM
+#define ADAFLASH_LSE_ROWS_PER_SM 12  // S1 splits rows over a cluster until there are this many units per SM
+#endif
 
-// (max, sum of 2^{(x - max) * scale}) per thread, combined by warps then CTA.
-// Entries equal to -inf contribute nothing.
+#ifndef ADAFLASH_DRAW_MINBLOCKS
+#define ADAFLASH_DRAW_MINBLOCKS 8  // resident S2 CTAs per SM: 8 CTAs x 152 SMs hold 128+ requests at once
+#endif
+
+constexpr int kLseThreads = ADAFLASH_LSE_THREADS;
+constexpr int kLseUnroll = ADAFLASH_LSE_UNROLL;  // 16-byte loads in flight per thread
+constexpr int kLseMaxCluster = 8;
+constexpr int kDrawThreads = 256;  // per CTA
+constexpr int kDrawCluster = 8;    // CTAs per request
+
+// (max, sum of 2^{(x - max) * scale}); entries equal to -inf contribute nothing.
 struct MaxSum {
   float m, s;
 };
@@ -87,42 +110,97 @@ __device__ __forceinline__ void unpack16(const uint4& w, float (&x)[8]) {
   x[7] = bf16_hi(w.w);
 }
 
-// ln sum_v exp(x_v / T) of one row, computed by the whole CTA (red holds 2 * 32
-// floats).  Every thread gets the result.  The same sequence of operations for any
-// row of one type and alignment, so equal rows give equal results bit for bit.
+// Eight consecutive entries starting at v0 (a multiple of 8); 16-byte loads when
+// the row starts on a 16-byte boundary, else eight element loads.
 template <class DT>
-__device__ float row_lse(const uint8_t* row, int V, bool vec, float inv_t, float* red) {
-  const float scale = kLog2e * inv_t;
-  MaxSum a{kNegInf, 0.f};
-  int v0 = 0;
-  if (vec) {
-    constexpr int E = 16 / DT::kBytes;
-    const int nvec = V / E;
-    const uint4* rw = reinterpret_cast<const uint4*>(row);
-    int j = threadIdx.x;
-    for (; j + static_cast<int>(blockDim.x) < nvec; j += 2 * blockDim.x) {
-      const uint4 w0 = __ldcs(rw + j), w1 = __ldcs(rw + j + blockDim.x);
-      float x0[E], x1[E];
-      unpack16(w0, x0);
-      unpack16(w1, x1);
-      ms_add_group<E>(a, x0, scale);
-      ms_add_group<E>(a, x1, scale);
-    }
-    if (j < nvec) {
-      float x0[E];
-      unpack16(__ldcs(rw + j), x0);
-      ms_add_group<E>(a, x0, scale);
-    }
-    v0 = nvec * E;
+__device__ __forceinline__ void load8(const uint8_t* row, bool aligned16, int v0, float (&x)[8]) {
+  if (!aligned16) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = DT::load(row, v0 + e);
+    return;
   }
-  for (int v = v0 + threadIdx.x; v < V; v += blockDim.x) ms_add(a, DT::load(row, v), scale);
+  const uint4* p = reinterpret_cast<const uint4*>(row + static_cast<int64_t>(v0) * DT::kBytes);
+  if constexpr (DT::kBytes == 2) {
+    unpack16(__ldg(p), x);
+  } else {
+    float lo[4], hi[4];
+    unpack16(__ldg(p), lo);
+    unpack16(__ldg(p + 1), hi);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[e] = lo[e];
+      x[4 + e] = hi[e];
+    }
+  }
+}
+
+// (max, sum) of slice `rank` of `C` of one row, reduced over the CTA (red holds
+// 2 * 32 floats); the result is valid in every thread.  The row is cut into groups
+// of 8 entries (C contiguous slices of groups) and a tail of V mod 8 entries (rank
+// C - 1).  The order of operations depends only on V and C, not on the element
+// type or the row's alignment, so rows holding equal values give equal results.
+template <class DT>
+__device__ MaxSum slice_maxsum(const uint8_t* row, int V, int rank, int C, float scale, float* red) {
+  const int B = static_cast<int>(blockDim.x);
+  const int tid = static_cast<int>(threadIdx.x);
+  const bool a16 = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  const int ng = V >> 3;
+  const int per = (ng + C - 1) / C;
+  const int g0 = min(ng, rank * per), g1 = min(ng, g0 + per);
+  MaxSum a{kNegInf, 0.f};
+  int g = g0 + tid;
+  if (a16) {
+    // 16-byte words loaded first, unpacked as they are consumed
+    constexpr int W = DT::kBytes / 2;                    // words per 8-entry group
+    constexpr int U = kLseUnroll * 2 / DT::kBytes > 0 ? kLseUnroll * 2 / DT::kBytes : 1;  // same bytes in flight
+    const uint4* rw = reinterpret_cast<const uint4*>(row);
+    for (; g + (U - 1) * B < g1; g += U * B) {
+      uint4 raw[U][W];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int q = 0; q < W; ++q) raw[u][q] = __ldcs(rw + static_cast<int64_t>(g + u * B) * W + q);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float x[8];
+        if constexpr (W == 1) {
+          unpack16(raw[u][0], x);
+        } else {
+          float lo[4], hi[4];
+          unpack16(raw[u][0], lo);
+          unpack16(raw[u][W - 1], hi);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[e] = lo[e];
+            x[4 + e] = hi[e];
+          }
+        }
+        ms_add_group<8>(a, x, scale);
+      }
+    }
+  } else {
+    // rows off the 16-byte grid: element loads, two groups in flight per thread
+    for (; g + B < g1; g += 2 * B) {
+      float x[2][8];
+      load8<DT>(row, false, g << 3, x[0]);
+      load8<DT>(row, false, (g + B) << 3, x[1]);
+      ms_add_group<8>(a, x[0], scale);
+      ms_add_group<8>(a, x[1], scale);
+    }
+  }
+  for (; g < g1; g += B) {
+    float x[8];
+    load8<DT>(row, a16, g << 3, x);
+    ms_add_group<8>(a, x, scale);
+  }
+  if (rank == C - 1)
+    for (int v = (ng << 3) + tid; v < V; v += B) ms_add(a, DT::load(row, v), scale);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     MaxSum b{__shfl_xor_sync(0xffffffffu, a.m, off), __shfl_xor_sync(0xffffffffu, a.s, off)};
     a = ms_merge(a, b, scale);
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31, nw = B >> 5;
   if (lane == 0) {
     red[warp] = a.m;
     red[32 + warp] = a.s;
@@ -130,8 +208,24 @@ __device__ float row_lse(const uint8_t* row, int V, bool vec, float inv_t, float
   __syncthreads();
   MaxSum t{kNegInf, 0.f};
   for (int w = 0; w < nw; ++w) t = ms_merge(t, MaxSum{red[w], red[32 + w]}, scale);
-  // lse = m / T + ln(s)
-  return t.m * inv_t + logf(t.s);
+  return t;
+}
+
+// One 8-entry group from its 16-byte words (1 for bf16, 2 for fp32).
+template <class DT>
+__device__ __forceinline__ void unpack_group(const uint4* raw, float (&x)[8]) {
+  if constexpr (DT::kBytes == 2) {
+    unpack16(raw[0], x);
+  } else {
+    float lo[4], hi[4];
+    unpack16(raw[0], lo);
+    unpack16(raw[1], hi);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[e] = lo[e];
+      x[4 + e] = hi[e];
+    }
+  }
 }
 
 // p = exp(x / T - lse) for one entry.
@@ -139,152 +233,308 @@ __device__ __forceinline__ float prob_at(float x, float inv_t, float lse) {
   return ex2(fmaf(x, inv_t, -lse) * kLog2e);
 }
 
+__device__ __forceinline__ bool is_aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
 }  // namespace
 
 // ---- S1: log-sum-exp at temperature of every draft row and every target row ----
 template <class DZ, class DT>
-__global__ void __launch_bounds__(kLseThreads) lse_rows_kernel(const SampledParams P) {
+__global__ void __launch_bounds__(kLseThreads, ADAFLASH_LSE_MINBLOCKS) lse_rows_kernel(const SampledParams P, int C) {
   __shared__ float red[64];
-  const int b = static_cast<int>(blockIdx.x);
-  float lse;
+  __shared__ float part[2 * kLseMaxCluster];
+  // S2 may be scheduled as soon as every S1 CTA is running; it waits for S1's results.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int b = static_cast<int>(blockIdx.x) / C;
+  const int rank = static_cast<int>(blockIdx.x) % C;  // == %cluster_ctarank for a 1-D cluster of C
+  const float scale = kLog2e * P.inv_t;
+  MaxSum ms;
   if (b < P.N_d) {
-    lse = row_lse<DZ>(static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(b) * P.ld_z * DZ::kBytes, P.V,
-                      P.z_vec != 0, P.inv_t, red);
+    ms = slice_maxsum<DZ>(static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(b) * P.ld_z * DZ::kBytes, P.V,
+                          rank, C, scale, red);
   } else {
-    lse = row_lse<DT>(static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(b - P.N_d) * P.ld_t * DT::kBytes,
-                      P.V, P.t_vec != 0, P.inv_t, red);
+    ms = slice_maxsum<DT>(static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(b - P.N_d) * P.ld_t * DT::kBytes,
+                          P.V, rank, C, scale, red);
   }
-  if (threadIdx.x == 0) P.row_lse[b] = lse;
+  if (C == 1) {
+    if (threadIdx.x == 0) P.row_lse[b] = ms.m * P.inv_t + logf(ms.s);  // lse = m / T + ln(s)
+    return;
+  }
+  if (threadIdx.x == 0) {
+    float* dst = map_to_rank(part, 0u);
+    dst[2 * rank] = ms.m;
+    dst[2 * rank + 1] = ms.s;
+  }
+  cluster_sync_all();
+  if (rank == 0 && threadIdx.x == 0) {
+    MaxSum t{kNegInf, 0.f};
+    for (int r = 0; r < C; ++r) t = ms_merge(t, MaxSum{part[2 * r], part[2 * r + 1]}, scale);
+    P.row_lse[b] = t.m * P.inv_t + logf(t.s);
+  }
 }
 
-// ---- S2: the accept rule, one warp per request ----
+// ---- S2: the accept rule and the draw, one cluster of kDrawCluster CTAs per request ----
+//
+// The vocabulary is cut into one contiguous segment per warp of the cluster, each a
+// whole number of tiles of 32 x 8 entries (lane l of a tile holds entries 8l..8l+7,
+// so every load instruction of a warp reads consecutive 16-byte words).  The warp
+// sums give, in vocabulary order, each warp's prefix; the owner warp stages its
+// segment's weights in shared memory and walks it tile by tile.
 template <class DZ, class DT>
-__global__ void __launch_bounds__(256) sampled_accept_kernel(const SampledParams P) {
-  const int lane = threadIdx.x & 31;
-  const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (i >= P.R) return;
+__global__ void __launch_bounds__(kDrawThreads, ADAFLASH_DRAW_MINBLOCKS) sampled_draw_kernel(const SampledParams P,
+                                                                                              int seg_tiles) {
+  extern __shared__ float wbuf[];  // seg_tiles * 256 weights of the owner warp's segment
+  __shared__ float scan[kDrawThreads / 32];
+  __shared__ float ctot[2][kDrawCluster];  // per pass: every CTA's sum, written into every CTA
+  __shared__ int cown[kDrawCluster];       // every CTA's last candidate warp (or -1)
+  __shared__ int s_L, s_owner;
+  __shared__ float s_lse[2 * (ADAFLASH_MAX_K + 1)];  // lse of draft row d0+j and target row d0+i+j
+  const int i = static_cast<int>(blockIdx.x) / kDrawCluster;
+  const int rank = static_cast<int>(blockIdx.x) % kDrawCluster;  // == %cluster_ctarank
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int d0 = __ldg(P.doff + i), d1 = __ldg(P.doff + i + 1);
   const int k = d1 - d0;
+  const float inv_t = P.inv_t;
   bool ok = (k >= 1) && (k <= ADAFLASH_MAX_K) && (d0 >= 0) && (d1 <= P.N_d);
   if (i == 0 && d0 != 0) ok = false;
   if (i == P.R - 1 && d1 != P.N_d) ok = false;
-  if (!ok) {
-    if (lane == 0) {
-      P.accept_len[i] = -1;
-      P.next_token[i] = -1;
-      P.accept_rate[i] = -1.f;
-      flag_status(P.status, ADAFLASH_ERR_BAD_OFFSETS);
-    }
-    return;
-  }
-  bool reject = false, badtok = false;
-  if (lane < k) {
-    const int d = d0 + lane, s = d0 + i + lane;
+
+  // The accept rule, evaluated by warp 0 of every CTA of the cluster (identical
+  // inputs and instructions, so identical L); CTA 0 writes the outputs.  The
+  // inputs it reads are fetched before waiting for S1, whose row_lse it then needs.
+  const int d = d0 + lane, s = d0 + i + lane;
+  const bool mine = (warp == 0) && ok && (lane < k);
+  bool badtok = false;
+  float zx = 0.f, tx = 0.f, ua = 0.f;
+  if (mine) {
     const int x = __ldg(P.tokens + d);
     badtok = (x < 0) || (x >= P.V);
-    if (badtok) {
-      reject = true;
+    if (!badtok) {
+      zx = DZ::load(static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(d) * P.ld_z * DZ::kBytes, x);
+      tx = DT::load(static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(s) * P.ld_t * DT::kBytes, x);
+    }
+    ua = __ldg(P.u_accept + d);
+  }
+  const float w = fminf(fmaxf(__ldg(P.u_sample + i), 0.f), 1.f);  // NaN -> 0
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // row_lse comes from S1
+  if (warp == 0) {
+    if (!ok) {
+      if (lane == 0) {
+        if (rank == 0) {
+          P.accept_len[i] = -1;
+          P.next_token[i] = -1;
+          P.accept_rate[i] = -1.f;
+          flag_status(P.status, ADAFLASH_ERR_BAD_OFFSETS);
+        }
+        s_L = -1;
+      }
     } else {
-      const float zx = DZ::load(static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(d) * P.ld_z * DZ::kBytes, x);
-      const float tx = DT::load(static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(s) * P.ld_t * DT::kBytes, x);
-      const float p = prob_at(zx, P.inv_t, P.row_lse[d]);
-      const float q = prob_at(tx, P.inv_t, P.row_lse[P.N_d + s]);
-      reject = !(__ldg(P.u_accept + d) * p < q);
+      bool reject = badtok;
+      // lanes j < k hold the lse of the pair at position j, lane k that of the bonus row
+      const float lz = mine ? P.row_lse[d] : 0.f;
+      const float lt = (lane <= k) ? P.row_lse[P.N_d + s] : 0.f;
+      if (lane <= k) {
+        s_lse[2 * lane] = lz;
+        s_lse[2 * lane + 1] = lt;
+      }
+      if (mine && !badtok) reject = !(ua * prob_at(zx, inv_t, lz) < prob_at(tx, inv_t, lt));
+      const unsigned rj = __ballot_sync(0xffffffffu, reject);
+      const unsigned bt = __ballot_sync(0xffffffffu, badtok);
+      if (lane == 0) {
+        const int L = rj ? (__ffs(rj) - 1) : k;
+        if (rank == 0) {
+          P.accept_len[i] = L;
+          P.accept_rate[i] = __fdiv_rn(static_cast<float>(L), static_cast<float>(k));
+          if (bt) flag_status(P.status, ADAFLASH_ERR_BAD_TOKEN);
+        }
+        s_L = L;
+      }
     }
   }
-  const unsigned rj = __ballot_sync(0xffffffffu, reject);
-  const unsigned bt = __ballot_sync(0xffffffffu, badtok);
-  if (lane == 0) {
-    const int L = rj ? (__ffs(rj) - 1) : k;
-    P.accept_len[i] = L;
-    P.accept_rate[i] = __fdiv_rn(static_cast<float>(L), static_cast<float>(k));
-    if (bt) flag_status(P.status, ADAFLASH_ERR_BAD_TOKEN);
-  }
-}
+  __syncthreads();
+  const int L = s_L;
+  if (L < 0) return;  // malformed request: the whole cluster leaves before any cluster barrier
 
-// ---- S3: draw the emitted token, one CTA per request ----
-template <class DZ, class DT>
-__global__ void __launch_bounds__(kDrawThreads) sampled_draw_kernel(const SampledParams P) {
-  __shared__ float scan[kDrawThreads / 32];
-  __shared__ int s_mode, s_owner;
-  const int i = blockIdx.x;
-  const int L = P.accept_len[i];
-  if (L < 0) return;  // malformed request (flagged by S2)
-  const int d0 = __ldg(P.doff + i), d1 = __ldg(P.doff + i + 1);
-  const int k = d1 - d0;
   const int V = P.V;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // L < k: residual max(0, q - p) at the first rejected position; L = k: q at the bonus row
   int mode = (L < k) ? 0 : 1;
   const int dz = d0 + min(L, k - 1);  // draft row of the rejected position (unused when mode = 1)
   const int st = d0 + i + L;          // target row of the emitted position
   const uint8_t* zrow = static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(dz) * P.ld_z * DZ::kBytes;
   const uint8_t* trow = static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(st) * P.ld_t * DT::kBytes;
-  const float lse_z = P.row_lse[dz];
-  const float lse_t = P.row_lse[P.N_d + st];
-  const int per = (V + kDrawThreads - 1) / kDrawThreads;
-  const int c0 = min(V, tid * per), c1 = min(V, c0 + per);
-  const float w = fminf(fmaxf(__ldg(P.u_sample + i), 0.f), 1.f);  // NaN -> 0
+  const bool z16 = is_aligned16(zrow), t16 = is_aligned16(trow);
+  const float lse_z = s_lse[2 * min(L, k - 1)];
+  const float lse_t = s_lse[2 * L + 1];
+  const int seg = seg_tiles * 256;                     // entries per warp segment
+  const int gw = rank * (kDrawThreads / 32) + warp;    // warp index in vocabulary order
+  const int s0 = min(V, gw * seg), s1 = min(V, s0 + seg);
+  const int full_groups = V >> 3;                      // groups with all 8 entries in range
 
-  auto weight = [&](int v, int md) -> float {
-    const float q = prob_at(DT::load(trow, v), P.inv_t, lse_t);
+  auto weight_of = [&](float tv, float zv, int md) -> float {
+    const float q = prob_at(tv, inv_t, lse_t);
     if (md == 1) return q;
-    return fmaxf(q - prob_at(DZ::load(zrow, v), P.inv_t, lse_z), 0.f);
+    return fmaxf(q - prob_at(zv, inv_t, lse_z), 0.f);
+  };
+  // the 8 weights of group g (entries 8g .. 8g+7; those >= V weigh 0)
+  auto group_weights = [&](int g, int md, float (&wv)[8]) {
+    float tv[8], zv[8];
+    if (g < full_groups) {
+      load8<DT>(trow, t16, g << 3, tv);
+      if (md == 0) {
+        load8<DZ>(zrow, z16, g << 3, zv);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zv[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) wv[e] = weight_of(tv[e], zv[e], md);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int v = (g << 3) + e;
+        wv[e] = (v < V) ? weight_of(DT::load(trow, v), md == 0 ? DZ::load(zrow, v) : 0.f, md) : 0.f;
+      }
+    }
   };
 
   for (int pass = 0; pass < 2; ++pass) {
-    // fixed-order sum of this thread's contiguous chunk
+    // this lane's share of the warp segment: group lane of every tile, in order
     float own = 0.f;
-    for (int v = c0; v < c1; ++v) own += weight(v, mode);
-    // block inclusive scan of the chunk sums (warp shuffles, then warp totals)
-    float incw = own;
+    const int g0 = s0 >> 3, g1 = (s1 > s0) ? (s1 + 7) >> 3 : g0;  // an empty segment has no groups
+    int g = g0 + lane;
+    if (t16 && (mode == 1 || z16)) {
+      // on the 16-byte grid: the words of several tiles issued before any is used
+      constexpr int WT = DT::kBytes / 2, WZ = DZ::kBytes / 2;
+      constexpr int U = 8 / (WT + WZ);  // tiles per round
+      const uint4* tw = reinterpret_cast<const uint4*>(trow);
+      const uint4* zw = reinterpret_cast<const uint4*>(zrow);
+      for (; g + 32 * (U - 1) < min(g1, full_groups); g += 32 * U) {
+        uint4 rt[U][WT], rz[U][WZ];
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, incw, off);
-      if (lane >= off) incw += y;
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+          for (int q = 0; q < WT; ++q) rt[u][q] = __ldg(tw + static_cast<int64_t>(g + 32 * u) * WT + q);
+#pragma unroll
+          for (int q = 0; q < WZ; ++q)
+            rz[u][q] = (mode == 0) ? __ldg(zw + static_cast<int64_t>(g + 32 * u) * WZ + q) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          float tv[8], zv[8];
+          unpack_group<DT>(rt[u], tv);
+          unpack_group<DZ>(rz[u], zv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) own += weight_of(tv[e], zv[e], mode);
+        }
+      }
     }
-    float exclw = __shfl_up_sync(0xffffffffu, incw, 1);
-    if (lane == 0) exclw = 0.f;
+    for (; g < g1; g += 32) {
+      float wv[8];
+      group_weights(g, mode, wv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) own += wv[e];
+    }
+    // warp sum (fixed butterfly order), CTA prefix over warps, cluster prefix over CTAs
+    float wsum = own;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    if (lane == 0) scan[warp] = wsum;
     __syncthreads();
-    if (lane == 31) scan[warp] = incw;
-    __syncthreads();
-    float before = 0.f, total = 0.f;
+    float before_w = 0.f, cta_total = 0.f;
     for (int ww = 0; ww < kDrawThreads / 32; ++ww) {
-      if (ww < warp) before += scan[ww];
-      total += scan[ww];
+      if (ww < warp) before_w += scan[ww];
+      cta_total += scan[ww];
     }
-    const float excl = lane == 0 ? before : exclw + before;
+    if (tid < kDrawCluster) *map_to_rank(&ctot[pass][rank], static_cast<uint32_t>(tid)) = cta_total;
+    cluster_sync_all();
+    float before_c = 0.f, total = 0.f;
+    for (int r = 0; r < kDrawCluster; ++r) {
+      if (r < rank) before_c += ctot[pass][r];
+      total += ctot[pass][r];
+    }
+    const float excl = before_c + before_w;  // this warp's prefix
     if (total > 0.f || mode == 1) {
       const float target = w * total;
-      // The owner is the last thread with positive mass whose prefix does not pass
-      // the threshold.  The first such thread has prefix exactly 0, so one exists
-      // whenever total > 0, and rounding in the scan cannot leave it unassigned.
+      // The owner is the last warp (in vocabulary order) with positive mass whose
+      // prefix does not pass the threshold.  The first such warp has prefix exactly
+      // 0, so one exists whenever total > 0 whatever the rounding.
       if (tid == 0) s_owner = -1;
       __syncthreads();
-      if (own > 0.f && (excl <= target || !(target < total))) atomicMax(&s_owner, tid);
+      if (lane == 0 && wsum > 0.f && (excl <= target || !(target < total))) atomicMax(&s_owner, warp);
       __syncthreads();
-      if (tid == s_owner) {
-        float acc = excl;
-        int pick = -1, last = -1;
-        for (int v = c0; v < c1; ++v) {
-          const float wv = weight(v, mode);
-          if (wv > 0.f) last = v;
-          acc += wv;
-          if (acc > target) {
-            pick = v;
-            break;
+      if (tid < kDrawCluster) *map_to_rank(&cown[rank], static_cast<uint32_t>(tid)) = s_owner;
+      cluster_sync_all();  // the last cluster barrier: no remote writes after it
+      int orank = -1;
+      for (int r = 0; r < kDrawCluster; ++r)
+        if (cown[r] >= 0) orank = r;
+      if (orank < 0) {
+        if (rank == 0 && tid == 0) P.next_token[i] = -1;  // no mass at all (non-finite logits)
+      } else if (rank == orank && warp == cown[orank]) {
+        // stage the segment's weights (coalesced), then walk it tile by tile: lane sums
+        // of 8 entries, a warp scan, and the first lane whose running sum passes the
+        // threshold resolves within its 8 entries
+        const int ntiles = (s1 - s0 + 255) >> 8;
+        for (int t = 0; t < ntiles; ++t) {
+          float wv[8];
+          group_weights((s0 >> 3) + 32 * t + lane, mode, wv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) wbuf[(t << 8) + (lane << 3) + e] = wv[e];
+        }
+        __syncwarp();
+        float base = excl;
+        int pick = -1, lastpos = -1;
+        for (int t = 0; t < ntiles && pick < 0; ++t) {
+          const float* tw8 = wbuf + (t << 8) + (lane << 3);
+          float ls = 0.f;
+          int lp = -1;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            ls += tw8[e];
+            if (tw8[e] > 0.f) lp = (t << 8) + (lane << 3) + e;
+          }
+          float inc = ls;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += y;
+          }
+          const unsigned hit = __ballot_sync(0xffffffffu, base + inc > target);
+          if (hit) {
+            const int hl = __ffs(hit) - 1;
+            int pk = -1;
+            if (lane == hl) {
+              float acc = base + inc - ls;
+              for (int e = 0; e < 8; ++e) {
+                acc += tw8[e];
+                if (acc > target) {
+                  pk = (t << 8) + (lane << 3) + e;
+                  break;
+                }
+              }
+              if (pk < 0) pk = lp;
+            }
+            pk = __shfl_sync(0xffffffffu, pk, hl);
+            // a run with no positive entry: the last positive one before it
+            const unsigned pos = __ballot_sync(0xffffffffu, lp >= 0) & (0xffffffffu >> (31 - hl));
+            if (pk < 0 && pos) pk = __shfl_sync(0xffffffffu, lp, 31 - __clz(pos));
+            if (pk < 0) pk = lastpos;
+            pick = pk;
+          } else {
+            const unsigned pos = __ballot_sync(0xffffffffu, lp >= 0);
+            if (pos) lastpos = __shfl_sync(0xffffffffu, lp, 31 - __clz(pos));
+            base += __shfl_sync(0xffffffffu, inc, 31);
           }
         }
-        P.next_token[i] = pick < 0 ? last : pick;
-      } else if (tid == 0 && s_owner < 0) {
-        P.next_token[i] = -1;  // no mass at all (non-finite logits)
+        if (pick < 0) pick = lastpos;  // the threshold lies past every partial sum
+        if (lane == 0) P.next_token[i] = s0 + max(pick, 0);
       }
       break;
     }
-    // residual of identical distributions is all zero: draw from q instead
-    if (tid == 0) s_mode = 1;
-    __syncthreads();
-    mode = s_mode;
+    // residual of identical distributions is all zero (the same verdict in every
+    // CTA): draw from q instead
+    mode = 1;
+    __syncthreads();  // scan[] is rewritten by the next pass
   }
 }
 
@@ -292,28 +542,61 @@ __global__ void __launch_bounds__(kDrawThreads) sampled_draw_kernel(const Sample
 // host side
 // ---------------------------------------------------------------------------
 
-template <class DZ, class DT>
-static cudaError_t launch_sampled_t(const SampledParams& p, cudaStream_t s) {
-  if (p.R <= 0) return cudaSuccess;
-  count_launch();
-  lse_rows_kernel<DZ, DT><<<static_cast<unsigned>(p.N_d + p.N_t), kLseThreads, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  count_launch();
-  sampled_accept_kernel<DZ, DT><<<static_cast<unsigned>((p.R * 32 + 255) / 256), 256, 0, s>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  count_launch();
-  sampled_draw_kernel<DZ, DT><<<static_cast<unsigned>(p.R), kDrawThreads, 0, s>>>(p);
-  return cudaGetLastError();
+static int lse_cluster_size(int rows, int num_sms) {
+  int C = 1;
+  while (C < kLseMaxCluster &&
+         static_cast<int64_t>(rows) * C < static_cast<int64_t>(ADAFLASH_LSE_ROWS_PER_SM) * num_sms)
+    C *= 2;
+  return C;
 }
 
-cudaError_t launch_sampled(const SampledParams& p, int z_dtype, int t_dtype, cudaStream_t s) {
+template <class DZ, class DT>
+static cudaError_t launch_sampled_t(const SampledParams& p, int num_sms, cudaStream_t s) {
+  if (p.R <= 0) return cudaSuccess;
+  const int rows = p.N_d + p.N_t;
+  const int C = lse_cluster_size(rows, num_sms);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(rows * C));
+    cfg.blockDim = dim3(kLseThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    count_launch();
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, lse_rows_kernel<DZ, DT>, p, C);
+    if (e != cudaSuccess) return e;
+  }
+  const int warps = kDrawCluster * (kDrawThreads / 32);
+  const int seg_tiles = ((p.V + 255) / 256 + warps - 1) / warps;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.R * kDrawCluster));
+  cfg.blockDim = dim3(kDrawThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(seg_tiles) * 256 * sizeof(float);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kDrawCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, sampled_draw_kernel<DZ, DT>, p, seg_tiles);
+}
+
+cudaError_t launch_sampled(const SampledParams& p, int z_dtype, int t_dtype, int num_sms, cudaStream_t s) {
   const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
-  if (zb && tb) return launch_sampled_t<BF16, BF16>(p, s);
-  if (!zb && tb) return launch_sampled_t<F32, BF16>(p, s);
-  if (zb && !tb) return launch_sampled_t<BF16, F32>(p, s);
-  return launch_sampled_t<F32, F32>(p, s);
+  if (zb && tb) return launch_sampled_t<BF16, BF16>(p, num_sms, s);
+  if (!zb && tb) return launch_sampled_t<F32, BF16>(p, num_sms, s);
+  if (zb && !tb) return launch_sampled_t<BF16, F32>(p, num_sms, s);
+  return launch_sampled_t<F32, F32>(p, num_sms, s);
 }
 
 }  // namespace adaflash

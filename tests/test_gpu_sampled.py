@@ -26,7 +26,7 @@ from oracle.opd import log_sum_exp  # noqa: E402
 from oracle.sampling import inverse_cdf, residual, sampled_accept, softmax_t  # noqa: E402
 from parity_lib import THREADS, to_device  # noqa: E402
 from synth import make_workload, materialize  # noqa: E402
-from synth.workloads import custom  # noqa: E402
+from synth.workloads import bf16_bits_to_f32, custom, f32_to_bf16_bits  # noqa: E402
 
 ACCEPT_REL = 1e-5
 DRAW_REL = 1e-4
@@ -234,17 +234,27 @@ def test_edge_shapes(case):
     _run_and_check(materialize(custom(**case)), 0.9, seed=len(case["k"]))
 
 
-def _equal_pair_batch(vocab, k, dtype="fp32"):
-    """A batch whose paired target rows equal the draft rows (bit for bit)."""
-    b = materialize(custom(vocab=vocab, k=k, d_dtype=dtype, t_dtype=dtype))
+def _equal_pair_batch(vocab, k, d_dtype="fp32", t_dtype="fp32"):
+    """A batch whose paired target rows hold the draft rows' values (exactly, in either storage type)."""
+    b = materialize(custom(vocab=vocab, k=k, d_dtype=d_dtype, t_dtype=t_dtype))
     w = b.w
     for d in range(w.num_draft_rows):
-        b.target[w.pair_target_row(d)] = b.draft[d]
+        s = w.pair_target_row(d)
+        if d_dtype == t_dtype:
+            b.target[s] = b.draft[d]
+        elif d_dtype == "fp32":  # bf16 target: round once, store the rounded values in both
+            bits = f32_to_bf16_bits(b.draft[d, :vocab])
+            b.target[s, :vocab] = bits
+            b.draft[d, :vocab] = bf16_bits_to_f32(bits)
+        else:
+            b.target[s, :vocab] = bf16_bits_to_f32(b.draft[d, :vocab])
     return b
 
 
-def test_equal_rows_accept_everything_and_draw_from_bonus_row():
-    b = _equal_pair_batch(3001, [4, 16, 1, 7])
+@pytest.mark.parametrize("dtypes", [("fp32", "fp32"), ("fp32", "bf16"), ("bf16", "fp32"), ("bf16", "bf16")])
+def test_equal_rows_accept_everything_and_draw_from_bonus_row(dtypes):
+    # V = 3001: consecutive rows start at different 16-byte alignments
+    b = _equal_pair_batch(3001, [4, 16, 1, 7], *dtypes)
     w = b.w
     u = np.full(w.num_draft_rows, np.float32(np.nextafter(np.float32(1), np.float32(0))))
     ws = np.random.default_rng(3).random(w.num_requests, dtype=np.float32)
@@ -252,6 +262,9 @@ def test_equal_rows_accept_everything_and_draw_from_bonus_row():
     assert run.status_word == 0
     assert np.array_equal(run.h["accept_len"], w.k)
     assert (run.h["accept_rate"] == 1.0).all()
+    Nd = w.num_draft_rows
+    for d in range(Nd):
+        assert run.h["row_lse"][d] == run.h["row_lse"][Nd + w.pair_target_row(d)], d
     check_all(b, 1.1, u, ws, run)
 
 
