@@ -30,12 +30,30 @@ METRIC = "logit rows/s for fused verify + clipped reverse-KL fwd/bwd; % of HBM p
 FALLBACK_HBM_GBS = 6800.0
 
 
-def source_hash() -> str:
+SAMPLED_T = 0.8  # temperature of the sampled-verification measurement
+
+
+# Sources that decide each kernel's code; a recorded ncu figure is used only while they are unchanged.
+KERNEL_SOURCES = {
+    "rowpass_kernel": ("rowpass.cu", "common.cuh", "kernels.h"),
+    "bwd_kernel": ("backward.cu", "common.cuh", "kernels.h"),
+    "lse_rows_kernel": ("sampled.cu", "common.cuh", "kernels.h"),
+    "sampled_draw_kernel": ("sampled.cu", "common.cuh", "kernels.h"),
+}
+
+
+def source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "serving_packed_var_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "serving_packed_var_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
+
+
+def _sum_traffic(traffic, names):
+    if not all(n in traffic for n in names):
+        return None
+    return sum(traffic[n]["dram_bytes_per_launch"] for n in names)
 
 
 def hbm_peak():
@@ -48,16 +66,15 @@ def hbm_peak():
 
 
 def ncu_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if the kernels are unchanged since."""
+    """Per-launch DRAM bytes from the committed ncu summary, for the kernels unchanged since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except Exception:
         return {}
-    if rec.get("source_sha") != source_hash():
-        return {}
-    return rec.get("kernels", {})
+    return {k: v for k, v in rec.get("kernels", {}).items()
+            if k in KERNEL_SOURCES and v.get("source_sha") == source_hash(k)}
 
 
 class ClockSampler:
@@ -289,6 +306,22 @@ def run_ours(args):
     torch.cuda.synchronize()
     fwd_alone_ms = fa.elapsed_time(fb_) / Kf
 
+    # temperature-sampled verification of the same batch (seeded uniforms, T = 0.8), calls back to back
+    urng = np.random.default_rng(1000 + rank)
+    u_acc = torch.from_numpy(urng.random(Nd, dtype=np.float32)).to(dev)
+    u_smp = torch.from_numpy(urng.random(R, dtype=np.float32)).to(dev)
+    sout = af.adaflash_verify_sampled(z, t, tok, doff, SAMPLED_T, u_acc, u_smp, status=status)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sa.record(stream)
+    for _ in range(Kf):
+        sout = af.adaflash_verify_sampled(z, t, tok, doff, SAMPLED_T, u_acc, u_smp, out=sout, status=status)
+    sb.record(stream)
+    torch.cuda.synchronize()
+    sampled_ms = sa.elapsed_time(sb) / Kf
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
     # end to end: pinned host inputs -> device, step, verify outputs + loss back to host
     e2e = run_e2e(args, b, w, dev, af, torch, np)
 
@@ -313,6 +346,10 @@ def run_ours(args):
                       "rows_per_s": Nd / (fwd_alone_ms * 1e-3)},
         "bwd": {"kernels": "bwd (K3)", "ms": bwd_ms, "bytes": bb, "achieved_gbs": bwd_gbs, "frac": bwd_gbs / peak,
                 "rows_per_s": Nd / (bwd_ms * 1e-3)},
+        "sampled_verify": {"kernels": f"lse_rows (S1) + accept/draw (S2), T = {SAMPLED_T}, calls back to back",
+                           "ms": sampled_ms, "bytes": fb, "achieved_gbs": fb / (sampled_ms * 1e-3) / 1e9,
+                           "frac": fb / (sampled_ms * 1e-3) / 1e9 / peak, "rows_per_s": Nd / (sampled_ms * 1e-3),
+                           "traffic": _sum_traffic(traffic, ("lse_rows_kernel", "sampled_draw_kernel"))},
     }
     dom = "bwd" if bwd_ms >= fwd_ms else "fwd_pass"
     tr_key = "bwd_kernel" if dom == "bwd" else "rowpass_kernel"
