@@ -145,6 +145,31 @@ adaflash_status adaflash_opd_loss_bwd(
     uint32_t* d_status, void* stream);
 
 /*
+ * adaflash_opd_loss_fwd_bwd -- the forward and the backward in one call.
+ *
+ * The drafter takes a training step right after each verification round (AdaFlash
+ * article, "On-Policy Distillation (OPD) for Domain Adaptation"), so the upstream
+ * weights are known when the forward runs.  Outputs and arguments are those of
+ * adaflash_opd_loss_fwd followed by adaflash_opd_loss_bwd with the same clip_c,
+ * ce_weight, grad_row and grad_scale, and so are the values, bit for bit.  When
+ * every row of draft_logits, target_logits and grad_draft starts on a 16-byte
+ * boundary and a row pair fits in the shared memory of a cluster of at most 8 CTAs,
+ * each logit is read from HBM once for both passes (the row pair stays on chip
+ * while its statistics are combined, then dz is written from there); otherwise
+ * the call runs the separate forward and backward kernels.
+ */
+adaflash_status adaflash_opd_loss_fwd_bwd(
+    const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
+    const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
+    const int32_t* draft_tokens, const int32_t* draft_offsets,
+    int32_t num_requests, int32_t num_draft_rows, int32_t vocab,
+    float clip_c, float ce_weight, const float* grad_row, float grad_scale,
+    int32_t* target_argmax, int32_t* accept_len, int32_t* bonus_token, float* accept_rate,
+    float* kl_row, float* ce_row, float* row_stats, float* loss,
+    float* grad_draft, int64_t ld_g,
+    uint32_t* d_status, void* stream);
+
+/*
  * adaflash_verify_sampled -- temperature-sampled verification of packed draft blocks.
  *
  * The target verifies the drafted tokens in parallel (AdaFlash article, opening

@@ -30,6 +30,7 @@ __all__ = [
     "adaflash_verify_packed",
     "adaflash_opd_loss_fwd",
     "adaflash_opd_loss_bwd",
+    "adaflash_opd_loss_fwd_bwd",
     "adaflash_verify_sampled",
     "adaflash_selftest_bounded_wait",
     "adaflash_status_string",
@@ -167,6 +168,42 @@ def adaflash_opd_loss_bwd(draft_logits, target_logits, draft_offsets, target_arg
         _ptr(grad_row), float(grad_scale), gp, ldg, _ptr(status), _stream(stream))
     _check(code, "adaflash_opd_loss_bwd")
     return g
+
+
+def adaflash_opd_loss_fwd_bwd(draft_logits, target_logits, draft_tokens, draft_offsets, clip_c, ce_weight=1.0,
+                              grad_row=None, grad_scale=1.0, vocab=None, out=None, status=None, stream=None):
+    """Forward and backward in one call.
+
+    Returns dict(target_argmax, accept_len, bonus_token, accept_rate, kl_row, ce_row, row_stats, loss, grad).
+    """
+    zp, ldz = _rows(draft_logits, "draft_logits")
+    tp, ldt = _rows(target_logits, "target_logits")
+    dev = draft_logits.device
+    R = draft_offsets.numel() - 1
+    Nd = draft_tokens.numel()
+    V = draft_logits.shape[1] if vocab is None else vocab
+    o = dict(out or {})
+    o.setdefault("target_argmax", _i32(Nd + R, dev))
+    o.setdefault("accept_len", _i32(R, dev))
+    o.setdefault("bonus_token", _i32(R, dev))
+    o.setdefault("accept_rate", _f32(R, dev))
+    o.setdefault("kl_row", _f32(Nd, dev))
+    o.setdefault("ce_row", _f32(Nd, dev))
+    o.setdefault("row_stats", torch.empty((Nd, 4), dtype=torch.float32, device=dev))
+    o.setdefault("loss", _f32(1, dev))
+    o.setdefault("grad", torch.empty((Nd, V), dtype=torch.float32, device=dev))
+    gp, ldg = _rows(o["grad"], "grad")
+    if o["grad"].dtype != torch.float32:
+        raise TypeError("grad must be float32")
+    code = _native.lib().adaflash_opd_loss_fwd_bwd(
+        zp, _dtype_code(draft_logits), ldz, tp, _dtype_code(target_logits), ldt,
+        draft_tokens.data_ptr(), draft_offsets.data_ptr(), R, Nd, V, float(clip_c), float(ce_weight),
+        _ptr(grad_row), float(grad_scale),
+        o["target_argmax"].data_ptr(), o["accept_len"].data_ptr(), o["bonus_token"].data_ptr(),
+        o["accept_rate"].data_ptr(), o["kl_row"].data_ptr(), o["ce_row"].data_ptr(), o["row_stats"].data_ptr(),
+        o["loss"].data_ptr(), gp, ldg, _ptr(status), _stream(stream))
+    _check(code, "adaflash_opd_loss_fwd_bwd")
+    return o
 
 
 def adaflash_verify_sampled(draft_logits, target_logits, draft_tokens, draft_offsets, temperature, u_accept,

@@ -37,6 +37,8 @@ SIGNATURES = {
                               _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "adaflash_opd_loss_bwd": [_vp, _i32, _i64, _vp, _i32, _i64, _vp, _i32, _i32, _i32, _f32, _f32,
                               _vp, _vp, _vp, _f32, _vp, _i64, _vp, _vp],
+    "adaflash_opd_loss_fwd_bwd": [_vp, _i32, _i64, _vp, _i32, _i64, _vp, _vp, _i32, _i32, _i32, _f32, _f32,
+                                  _vp, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp],
     "adaflash_verify_sampled": [_vp, _i32, _i64, _vp, _i32, _i64, _vp, _vp, _i32, _i32, _i32, _f32,
                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "adaflash_selftest_bounded_wait": [_vp, _i32, _vp],

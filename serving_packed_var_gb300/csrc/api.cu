@@ -264,6 +264,113 @@ adaflash_status adaflash_opd_loss_bwd(const void* draft_logits, adaflash_dtype d
   return ADAFLASH_OK;
 }
 
+adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
+                                          const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
+                                          const int32_t* draft_tokens, const int32_t* draft_offsets,
+                                          int32_t num_requests, int32_t num_draft_rows, int32_t vocab, float clip_c,
+                                          float ce_weight, const float* grad_row, float grad_scale,
+                                          int32_t* target_argmax, int32_t* accept_len, int32_t* bonus_token,
+                                          float* accept_rate, float* kl_row, float* ce_row, float* row_stats,
+                                          float* loss, float* grad_draft, int64_t ld_g, uint32_t* d_status,
+                                          void* stream) {
+  ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  ADAFLASH_TRY(check_logits(draft_logits, d_dtype, ld_d, vocab));
+  ADAFLASH_TRY(check_logits(target_logits, t_dtype, ld_t, vocab));
+  if (!int_ptr_ok(draft_tokens) || !int_ptr_ok(draft_offsets) || !int_ptr_ok(target_argmax) ||
+      !int_ptr_ok(accept_len) || !int_ptr_ok(bonus_token) || !int_ptr_ok(accept_rate) || !int_ptr_ok(kl_row) ||
+      !int_ptr_ok(ce_row) || !int_ptr_ok(row_stats) || !int_ptr_ok(loss) || !int_ptr_ok(grad_draft) || ld_g < vocab)
+    return ADAFLASH_ERR_INVALID_ARG;
+  if (grad_row && !aligned(grad_row, 4)) return ADAFLASH_ERR_INVALID_ARG;
+  if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
+  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight) || !std::isfinite(grad_scale)) return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_device());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_requests == 0) {
+    ADAFLASH_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
+    return ADAFLASH_OK;
+  }
+
+  RowPassParams p = {};
+  p.z = draft_logits;
+  p.t = target_logits;
+  p.ld_z = ld_d;
+  p.ld_t = ld_t;
+  p.doff = draft_offsets;
+  p.R = num_requests;
+  p.N_d = num_draft_rows;
+  p.N_t = num_draft_rows + num_requests;
+  p.V = vocab;
+  p.mode = kModeFwd;
+  p.clip_c = clip_c;
+  p.target_argmax = target_argmax;
+  p.kl_row = kl_row;
+  p.ce_row = ce_row;
+  p.row_stats = row_stats;
+  p.status = d_status;
+  p.ce_weight = ce_weight;
+  p.grad_row = grad_row;
+  p.grad_scale = grad_scale;
+  p.grad = grad_draft;
+  p.ld_g = ld_g;
+  const bool fast = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
+                    rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)) && rows_16b(grad_draft, ld_g, 4);
+  const bool fused = fast && num_draft_rows + num_requests <= fused_max_units(vocab, d_dtype, t_dtype, num_sms());
+  if (fused) {
+    ADAFLASH_CUDA(launch_fused(p, d_dtype, t_dtype, num_sms(), s));
+  } else {
+    // rows off the 16-byte grid, a vocabulary too large to hold on chip, or a batch of
+    // more than a wave of row units: the streaming forward, then the streaming backward
+    p.cluster = rowpass_cluster_size(vocab, p.N_d + p.R, num_sms());
+    p.slice = rowpass_slice(vocab, p.cluster);
+    ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype,
+                                 rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
+                                     rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)),
+                                 s));
+  }
+
+  FinalizeParams f = {};
+  f.tokens = draft_tokens;
+  f.doff = draft_offsets;
+  f.target_argmax = target_argmax;
+  f.R = num_requests;
+  f.N_d = num_draft_rows;
+  f.V = vocab;
+  f.accept_len = accept_len;
+  f.bonus_token = bonus_token;
+  f.accept_rate = accept_rate;
+  f.kl_row = kl_row;
+  f.ce_row = ce_row;
+  f.ce_weight = ce_weight;
+  f.loss = loss;
+  f.status = d_status;
+  ADAFLASH_CUDA(launch_finalize(f, s));
+
+  if (!fused) {
+    BwdParams b = {};
+    b.z = draft_logits;
+    b.t = target_logits;
+    b.ld_z = ld_d;
+    b.ld_t = ld_t;
+    b.doff = draft_offsets;
+    b.R = num_requests;
+    b.N_d = num_draft_rows;
+    b.N_t = num_draft_rows + num_requests;
+    b.V = vocab;
+    b.clip_c = clip_c;
+    b.ce_weight = ce_weight;
+    b.target_argmax = target_argmax;
+    b.row_stats = row_stats;
+    b.grad_row = grad_row;
+    b.grad_scale = grad_scale;
+    b.grad = grad_draft;
+    b.ld_g = ld_g;
+    b.chunks_per_row = (vocab + kBwdChunk - 1) / kBwdChunk;
+    b.status = d_status;
+    ADAFLASH_CUDA(launch_bwd(b, d_dtype, t_dtype, fast, s));
+  }
+  return ADAFLASH_OK;
+}
+
 adaflash_status adaflash_verify_sampled(const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
                                         const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
                                         const int32_t* draft_tokens, const int32_t* draft_offsets,

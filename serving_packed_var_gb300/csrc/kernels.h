@@ -28,6 +28,12 @@ struct RowPassParams {
   float* ce_row;
   float* row_stats;
   uint32_t* status;
+  // fused forward + backward only (K4)
+  float ce_weight;
+  const float* grad_row;  // NULL: grad_scale for every row
+  float grad_scale;
+  float* grad;            // [N_d, ld_g] float32
+  int64_t ld_g;
 };
 
 struct FinalizeParams {
@@ -86,6 +92,12 @@ void count_launch();
 cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
+// Fused forward + backward (K4).  fused_max_units is the largest batch (draft rows +
+// requests) the fused kernel is used for: 0 when a row pair does not fit a cluster's
+// shared memory; above it the caller runs K1 + K3, which stream faster on full waves.
+cudaError_t launch_fused(const RowPassParams& p, int z_dtype, int t_dtype, int num_sms, cudaStream_t s);
+int fused_cluster_size(int vocab, int bytes_per_entry);
+int fused_max_units(int vocab, int z_dtype, int t_dtype, int num_sms);
 cudaError_t launch_sampled(const SampledParams& p, int z_dtype, int t_dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t* status, int32_t limit_us, cudaStream_t s);
 

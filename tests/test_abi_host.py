@@ -92,6 +92,24 @@ def test_bwd_rejects(lib, kw):
     assert _bwd(lib, **kw) == INVALID
 
 
+def _fwdbwd(lib, **kw):
+    a = dict(z=FAKE, zd=1, ldz=1024, t=FAKE, td=1, ldt=1024, tok=FAKE, doff=FAKE, R=4, Nd=29, V=1024, c=1.0,
+             beta=1.0, grow=None, gs=1.0, loss=FAKE, g=FAKE, ldg=1024)
+    a.update(kw)
+    return lib.adaflash_opd_loss_fwd_bwd(a["z"], a["zd"], a["ldz"], a["t"], a["td"], a["ldt"], a["tok"], a["doff"],
+                                         a["R"], a["Nd"], a["V"], a["c"], a["beta"], a["grow"], a["gs"], FAKE, FAKE,
+                                         FAKE, FAKE, FAKE, FAKE, FAKE, a["loss"], a["g"], a["ldg"], None, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(z=None), dict(t=None), dict(tok=None), dict(doff=None), dict(loss=None), dict(g=None), dict(ldg=1000),
+    dict(g=FAKE + 2), dict(grow=FAKE + 1), dict(c=0.0), dict(c=float("nan")), dict(beta=float("inf")),
+    dict(gs=float("nan")), dict(zd=7), dict(ldz=5), dict(Nd=3), dict(R=-2),
+])
+def test_fwd_bwd_rejects(lib, kw):
+    assert _fwdbwd(lib, **kw) == INVALID
+
+
 def _sampled(lib, **kw):
     a = dict(z=FAKE, zd=1, ldz=1024, t=FAKE, td=1, ldt=1024, tok=FAKE, doff=FAKE, R=4, Nd=29, V=1024, T=1.0,
              ua=FAKE, us=FAKE, lse=FAKE, acc=FAKE, nxt=FAKE, rate=FAKE, status=None)
