@@ -23,10 +23,11 @@
  * base pointer and any ld >= vocab are accepted; rows whose start is 16-byte
  * aligned take the bulk-copy path, others a slower direct-load path.
  *
- * Ownership and ordering: every pointer argument is a DEVICE pointer owned by the
- * caller.  The library allocates nothing, keeps no state between calls and never
- * synchronises: each call enqueues its kernels on `stream` (a cudaStream_t; NULL is
- * the legacy default stream) and returns.  Calls on one stream run in order.
+ * Ownership and ordering: every pointer argument of the GPU entry points is a
+ * DEVICE pointer owned by the caller.  They allocate nothing, keep no state between
+ * calls and never synchronise: each call enqueues its kernels on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream) and returns.  Calls on one stream
+ * run in order.  The packer entry points (below) work on host memory only.
  *
  * Errors:
  *   - Argument errors found on the host are returned at once and nothing is
@@ -209,6 +210,46 @@ adaflash_status adaflash_verify_sampled(
     float temperature, const float* u_accept, const float* u_sample,
     float* row_lse, int32_t* accept_len, int32_t* next_token, float* accept_rate,
     uint32_t* d_status, void* stream);
+
+/*
+ * Variable-length request packing with an EMA capacity estimate (host side).
+ *
+ * The AdaFlash article ("Infrastructure: Async Training & Variable-Length Batching",
+ * "Variable-length request packing") packs requests of different predicted
+ * verification lengths into compact batches and sizes the next round with an
+ * exponential moving average, to use the GPU well without running out of memory.
+ * Reading: a request of predicted draft length k (1..16) occupies 2k + 1 logit rows
+ * (k draft rows, k + 1 target rows); a round holds at most row_budget rows; the
+ * estimate e of rows per request follows e <- alpha*x + (1 - alpha)*e with x a
+ * round's rows / requests (float64, that order); a round takes
+ * capacity = max(1, floor(row_budget / e)) requests from the front of the queue,
+ * gives back the last ones while their rows exceed row_budget, and packs the rest
+ * back to back.
+ *
+ * All pointers here are HOST pointers; nothing touches the GPU.  The packer is a
+ * small host object owned by the caller (create / destroy); calls on one packer
+ * must not run concurrently.
+ *
+ *   adaflash_packer_create   row_budget >= 33, 0 < alpha <= 1, initial estimate > 0
+ *   adaflash_packer_plan     queue_k int32 [n_queue] in 1..16 (queue order)    in
+ *                            draft_offsets int32 [n_queue + 1]                  out: [0..num_admitted] written
+ *                            num_admitted, capacity, rows (int32 each)          out
+ *                            the estimate is not changed
+ *   adaflash_packer_observe  a finished round's rows and requests: one EMA step (none if requests == 0)
+ *   adaflash_packer_estimate the current estimate of rows per request
+ * Errors: ADAFLASH_ERR_INVALID_ARG for NULL pointers, out-of-range arguments or a k
+ * outside 1..16 (nothing is written then).
+ */
+typedef struct adaflash_packer adaflash_packer;
+
+adaflash_status adaflash_packer_create(int32_t row_budget, double alpha, double initial_rows_per_request,
+                                       adaflash_packer** out);
+adaflash_status adaflash_packer_destroy(adaflash_packer* packer);
+adaflash_status adaflash_packer_plan(const adaflash_packer* packer, const int32_t* queue_k, int32_t n_queue,
+                                     int32_t* draft_offsets, int32_t* num_admitted, int32_t* capacity,
+                                     int32_t* rows);
+adaflash_status adaflash_packer_observe(adaflash_packer* packer, int32_t rows, int32_t requests);
+adaflash_status adaflash_packer_estimate(const adaflash_packer* packer, double* rows_per_request);
 
 /* Number of kernel launches this library has enqueued in this process so far
  * (all entry points, all devices).  For instrumentation: the difference over a

@@ -8,6 +8,9 @@ allocated with torch.  Every step of the computation runs in the CUDA kernels.
 
 from __future__ import annotations
 
+import ctypes
+
+import numpy as np
 import torch
 
 from . import _native
@@ -32,6 +35,7 @@ __all__ = [
     "adaflash_opd_loss_bwd",
     "adaflash_opd_loss_fwd_bwd",
     "adaflash_verify_sampled",
+    "Packer",
     "adaflash_selftest_bounded_wait",
     "adaflash_status_string",
     "adaflash_kernel_launches",
@@ -233,6 +237,52 @@ def adaflash_verify_sampled(draft_logits, target_logits, draft_tokens, draft_off
         o["next_token"].data_ptr(), o["accept_rate"].data_ptr(), _ptr(status), _stream(stream))
     _check(code, "adaflash_verify_sampled")
     return o
+
+
+class Packer:
+    """Host-side variable-length request packing with an EMA capacity estimate.
+
+    Wraps adaflash_packer_*: ``plan(queue_k)`` packs the front of a queue of predicted
+    draft lengths into one round (the estimate is unchanged); ``observe(rows, requests)``
+    takes one EMA step after a round.
+    """
+
+    def __init__(self, row_budget: int, alpha: float = 0.2, initial_rows_per_request: float = 17.0):
+        self._lib = _native.lib()
+        h = ctypes.c_void_p()
+        _check(self._lib.adaflash_packer_create(int(row_budget), float(alpha), float(initial_rows_per_request),
+                                                ctypes.byref(h)), "adaflash_packer_create")
+        self._h = h
+        self.row_budget = int(row_budget)
+
+    def plan(self, queue_k):
+        q = np.ascontiguousarray(np.asarray(queue_k, dtype=np.int32))
+        offs = np.zeros(len(q) + 1, dtype=np.int32)
+        na, cap, rows = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        code = self._lib.adaflash_packer_plan(self._h, q.ctypes.data if len(q) else None, len(q), offs.ctypes.data,
+                                              ctypes.byref(na), ctypes.byref(cap), ctypes.byref(rows))
+        _check(code, "adaflash_packer_plan")
+        return dict(admitted=na.value, draft_offsets=offs[:na.value + 1].copy(), capacity=cap.value, rows=rows.value)
+
+    def observe(self, rows: int, requests: int):
+        _check(self._lib.adaflash_packer_observe(self._h, int(rows), int(requests)), "adaflash_packer_observe")
+
+    @property
+    def estimate(self) -> float:
+        e = ctypes.c_double()
+        _check(self._lib.adaflash_packer_estimate(self._h, ctypes.byref(e)), "adaflash_packer_estimate")
+        return e.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.adaflash_packer_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def adaflash_selftest_bounded_wait(status, limit_us=1000, stream=None):

@@ -30,6 +30,7 @@ _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
 _i64 = ctypes.c_int64
 _f32 = ctypes.c_float
+_f64 = ctypes.c_double
 
 SIGNATURES = {
     "adaflash_verify_packed": [_vp, _i32, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp],
@@ -42,6 +43,11 @@ SIGNATURES = {
     "adaflash_verify_sampled": [_vp, _i32, _i64, _vp, _i32, _i64, _vp, _vp, _i32, _i32, _i32, _f32,
                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "adaflash_selftest_bounded_wait": [_vp, _i32, _vp],
+    "adaflash_packer_create": [_i32, _f64, _f64, _vp],
+    "adaflash_packer_destroy": [_vp],
+    "adaflash_packer_plan": [_vp, _vp, _i32, _vp, _vp, _vp, _vp],
+    "adaflash_packer_observe": [_vp, _i32, _i32],
+    "adaflash_packer_estimate": [_vp, _vp],
     "adaflash_status_string": [_i32],
     "adaflash_kernel_launches": [],
 }

@@ -17,7 +17,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libadaflash.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "rowpass.cu", "finalize.cu", "backward.cu", "sampled.cu", "fused.cu"]
+SOURCES = ["api.cu", "rowpass.cu", "finalize.cu", "backward.cu", "sampled.cu", "fused.cu", "packer.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I" + INCLUDE, "-I" + CSRC]
@@ -51,10 +51,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     def compile_one(src: str) -> str:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         if not force and _newer(o, [s] + headers):
             return o
-        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o]
+        # host C++ is compiled without floating-point contraction (results equal on x86 and Arm)
+        host = ["-Xcompiler", "-ffp-contract=off"] if src.endswith(".cpp") else []
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *host, *extra_flags, "-c", s, "-o", o]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
