@@ -212,6 +212,49 @@ adaflash_status adaflash_verify_sampled(
     uint32_t* d_status, void* stream);
 
 /*
+ * The logit-free forward: verification and OPD loss from final hidden states.
+ *
+ * A row's logits are its LM head applied to its final hidden state: z = W_d h_d for
+ * a draft row, t = W_t h_t for a target row.  adaflash_lmhead_opd_fwd produces every
+ * output of adaflash_opd_loss_fwd (same meaning, same layouts) from the hidden
+ * states and the two heads, without writing the logits: a tensor-core GEMM (tcgen05,
+ * bf16 x bf16 -> f32) reduces each 128-row x 256-entry tile of z and t to per-row
+ * statistics in the caller's workspace, a per-row pass combines them and
+ * re-evaluates exactly (dot products) only the entries whose clipped term can
+ * exceed clip_c, then the acceptance scan and the loss follow.
+ *
+ *   draft_hidden   bf16 [N_d, ld_hd]    in   (row d: the draft's hidden state at draft row d)
+ *   target_hidden  bf16 [N_t, ld_ht]    in   (packed like target_logits: N_t = N_d + R rows)
+ *   draft_head     bf16 [V, ld_wd]      in
+ *   target_head    bf16 [V, ld_wt]      in   (may be the same pointer as draft_head)
+ *   hidden         H, a multiple of 64; every ld >= H and a multiple of 8; every matrix
+ *                  16-byte aligned
+ *   workspace      device memory of at least adaflash_lmhead_workspace_bytes(R, N_d, V, H)
+ *                  bytes, 256-byte aligned, owned by the caller, overwritten
+ *   other arguments and outputs: as adaflash_opd_loss_fwd
+ * adaflash_lmhead_workspace_bytes returns -1 for invalid sizes.
+ *
+ * adaflash_lmhead_logits writes the logits of `rows` hidden rows under one head,
+ * logits[r, v] = sum_k h[r, k] w[v, k] (float32 [rows, ld_out]), with the same GEMM;
+ * it is there to check and time the tensor-core product on its own.
+ */
+int64_t adaflash_lmhead_workspace_bytes(int32_t num_requests, int32_t num_draft_rows, int32_t vocab, int32_t hidden);
+
+adaflash_status adaflash_lmhead_logits(const void* hidden_rows, int64_t ld_h, int32_t rows, const void* head,
+                                       int64_t ld_w, int32_t vocab, int32_t hidden, float* logits, int64_t ld_out,
+                                       uint32_t* d_status, void* stream);
+
+adaflash_status adaflash_lmhead_opd_fwd(
+    const void* draft_hidden, int64_t ld_hd, const void* target_hidden, int64_t ld_ht,
+    const void* draft_head, int64_t ld_wd, const void* target_head, int64_t ld_wt, int32_t hidden,
+    const int32_t* draft_tokens, const int32_t* draft_offsets,
+    int32_t num_requests, int32_t num_draft_rows, int32_t vocab,
+    float clip_c, float ce_weight, void* workspace, int64_t workspace_bytes,
+    int32_t* target_argmax, int32_t* accept_len, int32_t* bonus_token, float* accept_rate,
+    float* kl_row, float* ce_row, float* row_stats, float* loss,
+    uint32_t* d_status, void* stream);
+
+/*
  * Variable-length request packing with an EMA capacity estimate (host side).
  *
  * The AdaFlash article ("Infrastructure: Async Training & Variable-Length Batching",

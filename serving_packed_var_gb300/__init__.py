@@ -35,6 +35,9 @@ __all__ = [
     "adaflash_opd_loss_bwd",
     "adaflash_opd_loss_fwd_bwd",
     "adaflash_verify_sampled",
+    "adaflash_lmhead_logits",
+    "adaflash_lmhead_opd_fwd",
+    "adaflash_lmhead_workspace_bytes",
     "Packer",
     "adaflash_selftest_bounded_wait",
     "adaflash_status_string",
@@ -236,6 +239,68 @@ def adaflash_verify_sampled(draft_logits, target_logits, draft_tokens, draft_off
         u_accept.data_ptr(), u_sample.data_ptr(), o["row_lse"].data_ptr(), o["accept_len"].data_ptr(),
         o["next_token"].data_ptr(), o["accept_rate"].data_ptr(), _ptr(status), _stream(stream))
     _check(code, "adaflash_verify_sampled")
+    return o
+
+
+def _bf16_rows(t: torch.Tensor, name: str):
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    return _rows(t, name)
+
+
+def adaflash_lmhead_workspace_bytes(num_requests: int, num_draft_rows: int, vocab: int, hidden: int) -> int:
+    return int(_native.lib().adaflash_lmhead_workspace_bytes(int(num_requests), int(num_draft_rows), int(vocab),
+                                                             int(hidden)))
+
+
+def adaflash_lmhead_logits(hidden_rows, head, out=None, status=None, stream=None):
+    """logits[r, v] = sum_k hidden_rows[r, k] * head[v, k] (float32) with the tensor-core head GEMM."""
+    hp, ldh = _bf16_rows(hidden_rows, "hidden_rows")
+    wp, ldw = _bf16_rows(head, "head")
+    rows, H = hidden_rows.shape
+    V = head.shape[0]
+    if head.shape[1] != H:
+        raise ValueError("hidden sizes differ")
+    o = out if out is not None else torch.empty((rows, V), dtype=torch.float32, device=hidden_rows.device)
+    op, ldo = _rows(o, "out")
+    code = _native.lib().adaflash_lmhead_logits(hp, ldh, rows, wp, ldw, V, H, op, ldo, _ptr(status), _stream(stream))
+    _check(code, "adaflash_lmhead_logits")
+    return o
+
+
+def adaflash_lmhead_opd_fwd(draft_hidden, target_hidden, draft_head, target_head, draft_tokens, draft_offsets, clip_c,
+                            ce_weight=1.0, workspace=None, out=None, status=None, stream=None):
+    """Verification + OPD loss forward from final hidden states and LM heads (no logits written).
+
+    Returns dict(target_argmax, accept_len, bonus_token, accept_rate, kl_row, ce_row, row_stats, loss).
+    """
+    hdp, ldhd = _bf16_rows(draft_hidden, "draft_hidden")
+    htp, ldht = _bf16_rows(target_hidden, "target_hidden")
+    wdp, ldwd = _bf16_rows(draft_head, "draft_head")
+    wtp, ldwt = _bf16_rows(target_head, "target_head")
+    dev = draft_hidden.device
+    R = draft_offsets.numel() - 1
+    Nd = draft_tokens.numel()
+    V, H = target_head.shape
+    need = adaflash_lmhead_workspace_bytes(R, Nd, V, H)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    o = dict(out or {})
+    o.setdefault("target_argmax", _i32(Nd + R, dev))
+    o.setdefault("accept_len", _i32(R, dev))
+    o.setdefault("bonus_token", _i32(R, dev))
+    o.setdefault("accept_rate", _f32(R, dev))
+    o.setdefault("kl_row", _f32(Nd, dev))
+    o.setdefault("ce_row", _f32(Nd, dev))
+    o.setdefault("row_stats", torch.empty((Nd, 4), dtype=torch.float32, device=dev))
+    o.setdefault("loss", _f32(1, dev))
+    code = _native.lib().adaflash_lmhead_opd_fwd(
+        hdp, ldhd, htp, ldht, wdp, ldwd, wtp, ldwt, H, draft_tokens.data_ptr(), draft_offsets.data_ptr(), R, Nd, V,
+        float(clip_c), float(ce_weight), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        o["target_argmax"].data_ptr(), o["accept_len"].data_ptr(), o["bonus_token"].data_ptr(),
+        o["accept_rate"].data_ptr(), o["kl_row"].data_ptr(), o["ce_row"].data_ptr(), o["row_stats"].data_ptr(),
+        o["loss"].data_ptr(), _ptr(status), _stream(stream))
+    _check(code, "adaflash_lmhead_opd_fwd")
     return o
 
 

@@ -43,6 +43,10 @@ SIGNATURES = {
     "adaflash_verify_sampled": [_vp, _i32, _i64, _vp, _i32, _i64, _vp, _vp, _i32, _i32, _i32, _f32,
                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "adaflash_selftest_bounded_wait": [_vp, _i32, _vp],
+    "adaflash_lmhead_workspace_bytes": [_i32, _i32, _i32, _i32],
+    "adaflash_lmhead_logits": [_vp, _i64, _i32, _vp, _i64, _i32, _i32, _vp, _i64, _vp, _vp],
+    "adaflash_lmhead_opd_fwd": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _i32, _i32, _i32,
+                                _f32, _f32, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "adaflash_packer_create": [_i32, _f64, _f64, _vp],
     "adaflash_packer_destroy": [_vp],
     "adaflash_packer_plan": [_vp, _vp, _i32, _vp, _vp, _vp, _vp],
@@ -73,7 +77,8 @@ def lib() -> ctypes.CDLL:
         fn = getattr(L, name)
         fn.argtypes = args
         fn.restype = {"adaflash_status_string": ctypes.c_char_p,
-                      "adaflash_kernel_launches": ctypes.c_uint64}.get(name, ctypes.c_int)
+                      "adaflash_kernel_launches": ctypes.c_uint64,
+                      "adaflash_lmhead_workspace_bytes": ctypes.c_int64}.get(name, ctypes.c_int)
     _lib = L
     return L
 

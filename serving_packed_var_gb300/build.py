@@ -17,7 +17,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libadaflash.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "rowpass.cu", "finalize.cu", "backward.cu", "sampled.cu", "fused.cu", "packer.cpp"]
+SOURCES = ["api.cu", "rowpass.cu", "finalize.cu", "backward.cu", "sampled.cu", "fused.cu", "lmhead.cu", "packer.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I" + INCLUDE, "-I" + CSRC]

@@ -371,6 +371,148 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
   return ADAFLASH_OK;
 }
 
+// ---- LM-head path ----
+namespace {
+constexpr int kLmTileV = 256;  // vocabulary entries per tile of the head GEMM
+constexpr int kLmTileM = 128;
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+int64_t lm_ht_bytes(int64_t rows, int64_t H) { return round_up(rows * H * 2, 1024); }
+int64_t lm_partial_bytes(int64_t rows, int64_t V) {
+  return rows * ((V + kLmTileV - 1) / kLmTileV) * static_cast<int64_t>(sizeof(LmPartial));
+}
+
+adaflash_status check_bf16_rows(const void* p, int64_t ld, int32_t H) {
+  if (!p || !aligned(p, 16) || ld < H || ld % 8 != 0) return ADAFLASH_ERR_INVALID_ARG;
+  return ADAFLASH_OK;
+}
+}  // namespace
+
+int64_t adaflash_lmhead_workspace_bytes(int32_t num_requests, int32_t num_draft_rows, int32_t vocab, int32_t hidden) {
+  if (num_requests < 0 || num_draft_rows < 0 || vocab < 1 || hidden < 1) return -1;
+  const int64_t rows = static_cast<int64_t>(num_requests) + num_draft_rows;
+  return lm_ht_bytes(rows, hidden) + lm_partial_bytes(rows, vocab);
+}
+
+adaflash_status adaflash_lmhead_logits(const void* hidden_rows, int64_t ld_h, int32_t rows, const void* head,
+                                       int64_t ld_w, int32_t vocab, int32_t hidden, float* logits, int64_t ld_out,
+                                       uint32_t* d_status, void* stream) {
+  if (rows < 0 || vocab < 1 || vocab > ADAFLASH_MAX_VOCAB || hidden < 64 || hidden % 64 != 0)
+    return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_bf16_rows(hidden_rows, ld_h, hidden));
+  ADAFLASH_TRY(check_bf16_rows(head, ld_w, hidden));
+  if (!logits || !aligned(logits, 4) || ld_out < vocab) return ADAFLASH_ERR_INVALID_ARG;
+  if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_device());
+  if (rows == 0) return ADAFLASH_OK;
+  LmHeadParams p = {};
+  p.n_pair_tiles = 0;
+  p.n_pair_rows = 0;
+  p.n_t_rows = rows;
+  p.V = vocab;
+  p.H = hidden;
+  p.n_vtiles = (vocab + kLmTileV - 1) / kLmTileV;
+  p.mode = 1;
+  p.out_t = logits;
+  p.out_z = logits;
+  p.ld_out = ld_out;
+  p.status = d_status;
+  const uint16_t* h = static_cast<const uint16_t*>(hidden_rows);
+  const uint16_t* w = static_cast<const uint16_t*>(head);
+  ADAFLASH_CUDA(launch_lm_gemm(h, ld_h, h, ld_h, w, ld_w, w, ld_w, p, static_cast<cudaStream_t>(stream)));
+  return ADAFLASH_OK;
+}
+
+adaflash_status adaflash_lmhead_opd_fwd(const void* draft_hidden, int64_t ld_hd, const void* target_hidden,
+                                        int64_t ld_ht, const void* draft_head, int64_t ld_wd, const void* target_head,
+                                        int64_t ld_wt, int32_t hidden, const int32_t* draft_tokens,
+                                        const int32_t* draft_offsets, int32_t num_requests, int32_t num_draft_rows,
+                                        int32_t vocab, float clip_c, float ce_weight, void* workspace,
+                                        int64_t workspace_bytes, int32_t* target_argmax, int32_t* accept_len,
+                                        int32_t* bonus_token, float* accept_rate, float* kl_row, float* ce_row,
+                                        float* row_stats, float* loss, uint32_t* d_status, void* stream) {
+  ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  if (hidden < 64 || hidden % 64 != 0) return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_bf16_rows(draft_hidden, ld_hd, hidden));
+  ADAFLASH_TRY(check_bf16_rows(target_hidden, ld_ht, hidden));
+  ADAFLASH_TRY(check_bf16_rows(draft_head, ld_wd, hidden));
+  ADAFLASH_TRY(check_bf16_rows(target_head, ld_wt, hidden));
+  if (!int_ptr_ok(draft_tokens) || !int_ptr_ok(draft_offsets) || !int_ptr_ok(target_argmax) ||
+      !int_ptr_ok(accept_len) || !int_ptr_ok(bonus_token) || !int_ptr_ok(accept_rate) || !int_ptr_ok(kl_row) ||
+      !int_ptr_ok(ce_row) || !int_ptr_ok(row_stats) || !int_ptr_ok(loss))
+    return ADAFLASH_ERR_INVALID_ARG;
+  if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
+  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight)) return ADAFLASH_ERR_INVALID_ARG;
+  const int64_t need = adaflash_lmhead_workspace_bytes(num_requests, num_draft_rows, vocab, hidden);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_device());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_requests == 0) {
+    ADAFLASH_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
+    return ADAFLASH_OK;
+  }
+  const int32_t Nt = num_draft_rows + num_requests;
+  uint16_t* ht_pairs = static_cast<uint16_t*>(workspace);
+  LmPartial* partials =
+      reinterpret_cast<LmPartial*>(static_cast<uint8_t*>(workspace) + lm_ht_bytes(Nt, hidden));
+  ADAFLASH_CUDA(launch_lm_gather(static_cast<const uint16_t*>(target_hidden), ld_ht, draft_offsets, num_requests,
+                                 num_draft_rows, hidden, ht_pairs, d_status, s));
+  LmHeadParams p = {};
+  p.n_pair_tiles = (num_draft_rows + kLmTileM - 1) / kLmTileM;
+  p.n_pair_rows = num_draft_rows;
+  p.n_t_rows = Nt;
+  p.V = vocab;
+  p.H = hidden;
+  p.n_vtiles = (vocab + kLmTileV - 1) / kLmTileV;
+  p.mode = 0;
+  p.partials = partials;
+  p.status = d_status;
+  ADAFLASH_CUDA(launch_lm_gemm(static_cast<const uint16_t*>(draft_hidden), ld_hd, ht_pairs, hidden,
+                               static_cast<const uint16_t*>(draft_head), ld_wd,
+                               static_cast<const uint16_t*>(target_head), ld_wt, p, s));
+  LmCombineParams c = {};
+  c.hd = static_cast<const uint16_t*>(draft_hidden);
+  c.ht = ht_pairs;
+  c.wd = static_cast<const uint16_t*>(draft_head);
+  c.wt = static_cast<const uint16_t*>(target_head);
+  c.ld_hd = ld_hd;
+  c.ld_wd = ld_wd;
+  c.ld_wt = ld_wt;
+  c.doff = draft_offsets;
+  c.R = num_requests;
+  c.N_d = num_draft_rows;
+  c.V = vocab;
+  c.H = hidden;
+  c.n_vtiles = p.n_vtiles;
+  c.clip_c = clip_c;
+  c.partials = partials;
+  c.target_argmax = target_argmax;
+  c.kl_row = kl_row;
+  c.ce_row = ce_row;
+  c.row_stats = row_stats;
+  c.status = d_status;
+  ADAFLASH_CUDA(launch_lm_combine(c, s));
+
+  FinalizeParams f = {};
+  f.tokens = draft_tokens;
+  f.doff = draft_offsets;
+  f.target_argmax = target_argmax;
+  f.R = num_requests;
+  f.N_d = num_draft_rows;
+  f.V = vocab;
+  f.accept_len = accept_len;
+  f.bonus_token = bonus_token;
+  f.accept_rate = accept_rate;
+  f.kl_row = kl_row;
+  f.ce_row = ce_row;
+  f.ce_weight = ce_weight;
+  f.loss = loss;
+  f.status = d_status;
+  ADAFLASH_CUDA(launch_finalize(f, s));
+  return ADAFLASH_OK;
+}
+
 adaflash_status adaflash_verify_sampled(const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
                                         const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
                                         const int32_t* draft_tokens, const int32_t* draft_offsets,

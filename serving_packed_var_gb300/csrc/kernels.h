@@ -85,6 +85,46 @@ struct SampledParams {
   uint32_t* status;
 };
 
+// One row's statistics over one 256-entry vocabulary tile of the LM-head path.
+struct __align__(16) LmPartial {
+  float mz, sz, szd, dmax;  // max z, sum e^{z - mz}, sum e^{z - mz} (z - t), max (z - t)
+  float z2, mt, st;         // second largest z, max t, sum e^{t - mt}
+  int32_t az, at;           // first index of the largest z, of the largest t
+  float zat;                // z at that index of t
+  int32_t pad1, pad2;
+};
+
+struct LmHeadParams {
+  int32_t n_pair_tiles;  // 128-row tiles of (draft row, paired target row)
+  int32_t n_pair_rows;   // N_d
+  int32_t n_t_rows;      // rows of the target operand: N_d paired rows, then the bonus rows
+  int32_t V, H;
+  int32_t n_vtiles;
+  int32_t mode;          // 0: partial records, 1: write the logits (diagnostic)
+  LmPartial* partials;   // [n_t_rows][n_vtiles]
+  float* out_z;          // mode 1
+  float* out_t;
+  int64_t ld_out;
+  uint32_t* status;
+};
+
+struct LmCombineParams {
+  const uint16_t* hd;  // bf16 [N_d, ld_hd]
+  const uint16_t* ht;  // bf16 gathered target rows [N_d + R, H] (pair order, then bonus rows)
+  const uint16_t* wd;  // bf16 [V, ld_wd]
+  const uint16_t* wt;
+  int64_t ld_hd, ld_wd, ld_wt;
+  const int32_t* doff;
+  int32_t R, N_d, V, H, n_vtiles;
+  float clip_c;
+  const LmPartial* partials;
+  int32_t* target_argmax;
+  float* kl_row;
+  float* ce_row;
+  float* row_stats;
+  uint32_t* status;
+};
+
 // Launch counter behind adaflash_kernel_launches (incremented once per launch).
 void count_launch();
 
@@ -98,6 +138,14 @@ cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool fast, 
 cudaError_t launch_fused(const RowPassParams& p, int z_dtype, int t_dtype, int num_sms, cudaStream_t s);
 int fused_cluster_size(int vocab, int bytes_per_entry);
 int fused_max_units(int vocab, int z_dtype, int t_dtype, int num_sms);
+// LM-head path: gather of the target hidden rows into pair order (workspace), the
+// tcgen05 GEMM with its per-tile reduction (or logits), and the per-row combine.
+cudaError_t launch_lm_gather(const uint16_t* ht, int64_t ld_ht, const int32_t* doff, int R, int N_d, int H,
+                             uint16_t* out, uint32_t* status, cudaStream_t s);
+cudaError_t launch_lm_gemm(const uint16_t* hd, int64_t ld_hd, const uint16_t* ht_pairs, int64_t ld_ht,
+                           const uint16_t* wd, int64_t ld_wd, const uint16_t* wt, int64_t ld_wt,
+                           const LmHeadParams& p, cudaStream_t s);
+cudaError_t launch_lm_combine(const LmCombineParams& p, cudaStream_t s);
 cudaError_t launch_sampled(const SampledParams& p, int z_dtype, int t_dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t* status, int32_t limit_us, cudaStream_t s);
 

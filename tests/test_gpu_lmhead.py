@@ -1,0 +1,139 @@
+"""The logit-free path on the GPU: the tensor-core head GEMM (adaflash_lmhead_logits)
+against a float64 product, then adaflash_lmhead_opd_fwd against the oracle
+(oracle/lmhead.py), through the C ABI.
+
+Bars.  Logits: |d| <= 1e-5 (1 + sum_k |h_k w_k|) (float32 accumulation over H terms).
+Loss outputs: the bf16 bars of the logits path (2e-3 relative + 1e-5), S against its
+summands' size as there.  Argmax and the acceptance outputs are exact: the generator
+plants a target maximum at least ~25 logit units above the rest, far outside any
+rounding.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+from oracle import opd  # noqa: E402
+from oracle.lmhead import head_logits  # noqa: E402
+from synth.lmhead import custom_lmhead, make_lmhead_workload, materialize_lmhead  # noqa: E402
+from synth.workloads import bf16_bits_to_f32, f32_to_bf16_bits  # noqa: E402
+
+REL, ABS = 2e-3, 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rows,V,H", [(1, 256, 64), (200, 1000, 256), (128, 4096, 512), (37, 2049, 1024)])
+def test_head_gemm_matches_float64(rows, V, H):
+    import serving_packed_var_gb300 as af
+    rng = np.random.default_rng(rows + V + H)
+    hb = f32_to_bf16_bits(rng.standard_normal((rows, H), dtype=np.float32))
+    wb = f32_to_bf16_bits(rng.standard_normal((V, H), dtype=np.float32) * np.float32(0.05))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = af.adaflash_lmhead_logits(_dev_bf16(hb), _dev_bf16(wb), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    h, w = bf16_bits_to_f32(hb).astype(np.float64), bf16_bits_to_f32(wb).astype(np.float64)
+    ref = head_logits(h, w)
+    mag = np.abs(h) @ np.abs(w).T
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
+    assert (err <= 1e-5 * (1 + mag)).all(), float((err / (1 + mag)).max())
+
+
+def _run(b, clip_c=None):
+    import serving_packed_var_gb300 as af
+    w = b.w
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wd = _dev_bf16(b.wd)
+    wt = wd if b.wd is b.wt else _dev_bf16(b.wt)
+    out = af.adaflash_lmhead_opd_fwd(_dev_bf16(b.hd), _dev_bf16(b.ht), wd, wt, torch.from_numpy(b.tokens).cuda(),
+                                     torch.from_numpy(b.doff).cuda(), w.clip_c if clip_c is None else clip_c,
+                                     w.ce_weight, status=st)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}, int(st.item())
+
+
+def _check(b, h, rows, clip_c=None):
+    w = b.w
+    c = w.clip_c if clip_c is None else clip_c
+    hd, ht = b.f32("hd"), b.f32("ht")
+    wd, wt = b.f32("wd"), b.f32("wt")
+    for d in rows:
+        s = w.pair_target_row(d)
+        z = head_logits(hd[d], wd)[0]
+        t = head_logits(ht[s], wt)[0]
+        f = opd.row_forward(z, t, c, w.ce_weight)
+        for key, got in (("kl", h["kl_row"][d]), ("ce", h["ce_row"][d]), ("lse_z", h["row_stats"][d][0]),
+                         ("lse_t", h["row_stats"][d][1])):
+            assert abs(got - f[key]) <= REL * abs(f[key]) + ABS, (key, d, got, f[key])
+        assert abs(h["row_stats"][d][2] - f["S"]) <= REL * (abs(f["S"]) + f["S_l1"]) + ABS, ("S", d)
+        assert int(h["row_stats"][d][3]) == f["n_clipped"], ("n_clipped", d)
+        assert h["target_argmax"][s] == f["argmax"], ("argmax", d)
+
+
+def _check_verify(b, h):
+    w = b.w
+    for i in range(w.num_requests):
+        d0, k = int(b.doff[i]), int(w.k[i])
+        am = [int(b.spike_token[d0 + i + j]) for j in range(k + 1)]
+        L, bonus = opd.greedy_accept(b.tokens[d0:d0 + k], am)
+        assert h["accept_len"][i] == L == w.planted_accept[i], i
+        assert h["bonus_token"][i] == bonus, i
+        assert h["accept_rate"][i].view(np.uint32) == opd.acceptance_rate(L, k).view(np.uint32), i
+    assert np.array_equal(h["target_argmax"], b.spike_token), "target argmax"
+
+
+@pytest.mark.parametrize("clip_c", [1.0, 0.05, float("inf")])
+def test_tiny_every_row(clip_c):
+    b = materialize_lmhead(make_lmhead_workload("lm_tiny"))
+    h, st = _run(b, clip_c)
+    assert st == 0
+    _check_verify(b, h)
+    _check(b, h, range(b.w.num_draft_rows), clip_c)
+    w = b.w
+    rows = range(w.num_draft_rows)
+    fs = [opd.row_forward(head_logits(b.f32("hd")[d], b.f32("wd"))[0],
+                          head_logits(b.f32("ht")[w.pair_target_row(d)], b.f32("wt"))[0], clip_c, w.ce_weight)
+          for d in rows]
+    ref = sum(f["loss_row"] for f in fs) / len(fs)
+    assert abs(float(h["loss"][0]) - ref) <= REL * abs(ref) + ABS
+
+
+def test_small_shared_head():
+    b = materialize_lmhead(make_lmhead_workload("lm_small"))
+    h, st = _run(b)
+    assert st == 0
+    _check_verify(b, h)
+    _check(b, h, range(b.w.num_draft_rows))
+
+
+@pytest.mark.parametrize("case", [dict(vocab=300, hidden=64, k=[2, 1]), dict(vocab=5000, hidden=192, k=[16] * 9),
+                                  dict(vocab=257, hidden=128, k=[3, 16, 1, 7])])
+def test_edge_shapes(case):
+    b = materialize_lmhead(custom_lmhead(**case, shared_head=False))
+    h, st = _run(b)
+    assert st == 0
+    _check_verify(b, h)
+    _check(b, h, range(b.w.num_draft_rows))
+
+
+def test_qwen3_8b_shapes_c32_sampled_rows():
+    b = materialize_lmhead(make_lmhead_workload("lm_c32"))
+    h, st = _run(b)
+    assert st == 0
+    _check_verify(b, h)
+    nd = b.w.num_draft_rows
+    _check(b, h, sorted({0, 7, nd // 2, nd - 1}))
