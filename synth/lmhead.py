@@ -12,7 +12,9 @@ Recipe (all bfloat16, round to nearest even):
   gives logits of standard deviation about sigma;
 * draft head W_d = W_t (shared) or W_t + N(0, (head_noise * sigma / sqrt(H))^2);
 * target hidden row s: h_s ~ N(0, 1) plus (spike / sigma^2) * W_t[a_s] for a seeded
-  token a_s, which lifts logit a_s by about ``spike`` above the rest;
+  token a_s, which lifts logit a_s by about ``spike`` (chosen per vocabulary size so
+  that a_s stays the argmax by several standard deviations while the target still
+  puts visible mass elsewhere, and the draft much more);
 * draft hidden row d (paired with target row s): draft_scale * Ht[s] + N(0, draft_noise^2);
 * draft tokens: a_s for the planted accepted prefix j < L_i (a_s is the target's
   argmax by a wide margin), another token at j = L_i, uniform tokens after it.
@@ -47,8 +49,8 @@ class LMHeadWorkload:
     ce_weight: float = 1.0
     seed: int = 0
     shared_head: bool = True
-    sigma: float = 3.0
-    spike: float = 40.0
+    sigma: float = 2.5
+    spike: float = 18.0
     head_noise: float = 0.05
     draft_scale: float = 0.8
     draft_noise: float = 0.35
@@ -177,10 +179,10 @@ def make_lmhead_workload(name: str, seed: int = 0, **over) -> LMHeadWorkload:
     meta = _rng(seed, 1, 99)
     if name == "lm_tiny":
         k = np.array([16, 9, 3, 1], dtype=np.int32)
-        kw = dict(vocab=2048, hidden=256, shared_head=False)
+        kw = dict(vocab=2048, hidden=256, shared_head=False, spike=12.0)
     elif name == "lm_small":
         k = meta.integers(1, 17, size=8).astype(np.int32)
-        kw = dict(vocab=8192, hidden=512)
+        kw = dict(vocab=8192, hidden=512, spike=14.0)
     elif name == "lm_c32":
         k = meta.integers(1, 17, size=32).astype(np.int32)
         kw = dict(vocab=151936, hidden=4096)
@@ -199,6 +201,7 @@ def make_lmhead_workload(name: str, seed: int = 0, **over) -> LMHeadWorkload:
 
 def custom_lmhead(vocab: int, hidden: int, k, seed: int = 0, **over) -> LMHeadWorkload:
     meta = _rng(seed, 1, 98)
+    over.setdefault("spike", 12.0 if vocab <= 4096 else 14.0)
     k = np.asarray(k, dtype=np.int32)
     L = np.array([meta.integers(0, ki + 1) for ki in k], dtype=np.int32)
     return LMHeadWorkload(name=over.pop("name", "lm_custom"), vocab=vocab, hidden=hidden, k=k, planted_accept=L,

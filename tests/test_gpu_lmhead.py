@@ -4,9 +4,9 @@ against a float64 product, then adaflash_lmhead_opd_fwd against the oracle
 
 Bars.  Logits: |d| <= 1e-5 (1 + sum_k |h_k w_k|) (float32 accumulation over H terms).
 Loss outputs: the bf16 bars of the logits path (2e-3 relative + 1e-5), S against its
-summands' size as there.  Argmax and the acceptance outputs are exact: the generator
-plants a target maximum at least ~25 logit units above the rest, far outside any
-rounding.
+summands' size as there.  The target argmax is exact unless the oracle's two largest
+logits of a row lie within the GEMM's rounding (1e-4 (1 + max |t|)), where either is
+valid; the acceptance outputs are exact given the argmax.
 """
 
 import numpy as np
@@ -84,16 +84,35 @@ def _check(b, h, rows, clip_c=None):
         assert h["target_argmax"][s] == f["argmax"], ("argmax", d)
 
 
+def _oracle_target_argmax(b):
+    """First maximiser of every target row's float64 logits, and the runner-up gap."""
+    ht, wt = b.f32("ht"), b.f32("wt")
+    am, tops = [], []
+    for r0 in range(0, ht.shape[0], 256):
+        t = head_logits(ht[r0:r0 + 256], wt)
+        for row in t:
+            a = opd.first_argmax(row)
+            am.append(a)
+            tops.append(row)
+    return am, tops
+
+
 def _check_verify(b, h):
     w = b.w
+    am, tops = _oracle_target_argmax(b)
+    got = h["target_argmax"]
+    for s in range(w.num_target_rows):
+        if got[s] != am[s]:
+            row = tops[s]
+            assert row[got[s]] >= row[am[s]] - 1e-4 * (1 + abs(row[am[s]])), ("argmax", s, got[s], am[s])
+    # acceptance from the GPU's own argmax (exact given it)
     for i in range(w.num_requests):
         d0, k = int(b.doff[i]), int(w.k[i])
-        am = [int(b.spike_token[d0 + i + j]) for j in range(k + 1)]
-        L, bonus = opd.greedy_accept(b.tokens[d0:d0 + k], am)
-        assert h["accept_len"][i] == L == w.planted_accept[i], i
+        L, bonus = opd.greedy_accept(b.tokens[d0:d0 + k], [int(x) for x in got[d0 + i:d0 + i + k + 1]])
+        assert h["accept_len"][i] == L, i
         assert h["bonus_token"][i] == bonus, i
         assert h["accept_rate"][i].view(np.uint32) == opd.acceptance_rate(L, k).view(np.uint32), i
-    assert np.array_equal(h["target_argmax"], b.spike_token), "target argmax"
+    assert np.mean(np.asarray(got) == np.asarray(am)) > 0.99
 
 
 @pytest.mark.parametrize("clip_c", [1.0, 0.05, float("inf")])
@@ -102,6 +121,7 @@ def test_tiny_every_row(clip_c):
     h, st = _run(b, clip_c)
     assert st == 0
     _check_verify(b, h)
+    assert float(np.mean(h["kl_row"])) > 0.05 and float(np.mean(h["ce_row"])) > 0.05  # not a degenerate batch
     _check(b, h, range(b.w.num_draft_rows), clip_c)
     w = b.w
     rows = range(w.num_draft_rows)
