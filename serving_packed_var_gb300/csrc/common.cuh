@@ -241,6 +241,10 @@ __device__ __forceinline__ float warp_max_f32(float v) {
 }
 
 // Named barrier over the first `count` threads of the CTA (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync_id(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int count) {
   asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");
 }

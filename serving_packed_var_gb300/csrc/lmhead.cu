@@ -9,10 +9,10 @@
 //
 //   L0 gathers the target hidden rows into pair order (the target row paired with
 //      each draft row, then the bonus rows) in the caller's workspace;
-//   L1 is a tcgen05 GEMM: one CTA per (128-row tile, 256-entry vocabulary tile)
-//      computes the z and t tiles into TMEM (TMA loads of 128-byte-swizzled K-major
-//      operands into a 2-stage shared-memory ring, one thread issuing the MMAs),
-//      and its four epilogue warps reduce each row of the tile to a partial record:
+//   L1 is a persistent tcgen05 GEMM: per (128-row tile, 256-entry vocabulary tile)
+//      it computes the z and t tiles into TMEM (TMA loads of swizzled K-major
+//      operands into a shared-memory ring, one thread issuing the MMAs), and its
+//      epilogue warps reduce each row of the tile to a partial record:
 //      max, sum of exponentials, sum of e^z (z - t), max (z - t), the two largest z
 //      (with the index of the largest), the first index of the largest t and z there;
 //   L2 combines a row's records in a fixed order into its log-sum-exps, the
@@ -36,14 +36,26 @@ namespace adaflash {
 
 namespace {
 
+#ifndef ADAFLASH_LM_BK
+#define ADAFLASH_LM_BK 64  // hidden elements per k-block: 64 (128-byte swizzle, 2 stages) or 32 (64-byte, 4 stages)
+#endif
 constexpr int kBM = 128;  // rows per tile (TMEM lanes)
 constexpr int kBN = 256;  // vocabulary entries per tile
-constexpr int kBK = 64;   // hidden elements per k-block: one 128-byte swizzle row of bf16
-constexpr int kLStages = 2;
-constexpr int kLThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kBK = ADAFLASH_LM_BK;
+constexpr int kRowBytes = kBK * 2;  // one swizzle row
+// Stage layout: A_z, A_t, then B_z and B_t, or a single B when the two heads are the
+// same matrix (one weight tile feeds both products, and the ring has room for more stages).
+template <bool kShared>
+struct Ring {
+  static constexpr uint32_t kB = kBN * kBK * 2;
+  static constexpr uint32_t kA = kBM * kBK * 2;
+  static constexpr uint32_t kStage = 2 * kA + (kShared ? 1 : 2) * kB;
+  static constexpr int kStages = (kBK == 32 ? 2 : 1) * (kShared ? 3 : 2);
+  static constexpr uint32_t kOffBz = 2 * kA;
+  static constexpr uint32_t kOffBt = kShared ? 2 * kA : 2 * kA + kB;
+};
 constexpr uint32_t kTileA = kBM * kBK * 2;
 constexpr uint32_t kTileB = kBN * kBK * 2;
-constexpr uint32_t kStageBytes = 2 * kTileA + 2 * kTileB;
 constexpr uint32_t kTmemCols = 512;  // z tile in columns 0..255, t tile in 256..511
 constexpr int kCombThreads = 256;
 
@@ -54,67 +66,122 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }  // namespace
 
 // ---- L1: the head GEMM and the per-tile row reduction ----
-__global__ void __launch_bounds__(kLThreads, 1)
+//
+// Persistent: CTA c takes tiles c, c + G, ... (row tiles fastest, so the CTAs at
+// work at any time share weight tiles through L2).  The TMA warp runs ahead across
+// tiles; the MMA warp starts a tile once the epilogue has read the accumulators of
+// the previous one.  Sixteen epilogue warps split a tile: warp w reads TMEM lanes
+// 32 (w mod 4) .. +31 (the hardware's lane quarters) and a quarter of the 256
+// columns; the four quarter records of a row are merged in column order.
+
+namespace {
+
+constexpr int kEpiWarps = 16;
+constexpr int kGemmThreads = 64 + kEpiWarps * 32;
+
+struct EpiRec {
+  float mz, sz, szd, dmax, z2, mt, st, zat;
+  int az, at;
+};
+
+// Record b (columns after a's) merged into a: ties keep a's (lower) indices.
+__device__ __forceinline__ void epi_merge(EpiRec& a, const EpiRec& b) {
+  if (b.mz > a.mz) {
+    const float f = (a.mz == kNegInf) ? 0.f : ex2((a.mz - b.mz) * kLog2e);
+    a.sz = a.sz * f + b.sz;
+    a.szd = a.szd * f + b.szd;
+    a.z2 = fmaxf(a.mz, b.z2);
+    a.mz = b.mz;
+    a.az = b.az;
+  } else if (b.mz != kNegInf) {
+    const float f = ex2((b.mz - a.mz) * kLog2e);
+    a.sz = a.sz + b.sz * f;
+    a.szd = a.szd + b.szd * f;
+    a.z2 = fmaxf(a.z2, b.mz);
+  }
+  a.dmax = fmaxf(a.dmax, b.dmax);
+  if (b.mt > a.mt) {
+    const float f = (a.mt == kNegInf) ? 0.f : ex2((a.mt - b.mt) * kLog2e);
+    a.st = a.st * f + b.st;
+    a.mt = b.mt;
+    a.at = b.at;
+    a.zat = b.zat;
+  } else if (b.mt != kNegInf) {
+    a.st = a.st + b.st * ex2((b.mt - a.mt) * kLog2e);
+  }
+}
+
+}  // namespace
+
+template <bool kShared>
+__global__ void __launch_bounds__(kGemmThreads, 1)
     lmhead_gemm_kernel(const __grid_constant__ CUtensorMap map_hd, const __grid_constant__ CUtensorMap map_ht,
                        const __grid_constant__ CUtensorMap map_wd, const __grid_constant__ CUtensorMap map_wt,
                        const LmHeadParams P) {
   extern __shared__ uint8_t smem_raw[];
+  using RG = Ring<kShared>;
+  constexpr int kLStages = RG::kStages;
+  constexpr uint32_t kStageBytes = RG::kStage;
   __shared__ uint64_t full_bar[kLStages];
   __shared__ uint64_t empty_bar[kLStages];
-  __shared__ uint64_t accum_bar;
+  __shared__ uint64_t accum_full, accum_empty;
   __shared__ uint32_t tmem_base;
   __shared__ int s_err;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = static_cast<int>(blockIdx.x), vt = static_cast<int>(blockIdx.y);
-  const bool pair = mt < P.n_pair_tiles;
-  // first row of the tile in the target operand (pair rows are also draft rows)
-  const int row0 = pair ? mt * kBM : P.n_pair_rows + (mt - P.n_pair_tiles) * kBM;
-  const int row_end = pair ? P.n_pair_rows : P.n_t_rows;
-  const int v0 = vt * kBN;
+  const int m_tiles = P.n_pair_tiles + (P.n_t_rows - P.n_pair_rows + kBM - 1) / kBM;
+  const int n_tiles = m_tiles * P.n_vtiles;
   const int nkb = P.H / kBK;
   uint8_t* ring = align1024(smem_raw);
+  EpiRec* red = reinterpret_cast<EpiRec*>(ring + kLStages * kStageBytes);  // [4][kBM]
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kLStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(&accum_bar, 1);
+    mbar_init(&accum_full, 1);
+    mbar_init(&accum_empty, kEpiWarps);
     fence_barrier_init();
     s_err = 0;
     tma_prefetch_desc(&map_ht);
     tma_prefetch_desc(&map_wt);
-    if (pair) {
-      tma_prefetch_desc(&map_hd);
-      tma_prefetch_desc(&map_wd);
-    }
+    tma_prefetch_desc(&map_hd);
+    tma_prefetch_desc(&map_wd);
   }
   if (warp == 1) tmem_alloc(&tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  volatile int* err = &s_err;  // after a failed wait, every role stops waiting
 
   if (warp == 0) {
-    // ---- TMA producer ----
+    // ---- TMA producer: every k-block of every tile of this CTA ----
     if (lane == 0) {
-      const uint32_t bytes = pair ? kStageBytes : (kTileA + kTileB);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kLStages;
-        if (kb >= kLStages && !mbar_wait_bounded(&empty_bar[s], ((kb / kLStages) - 1) & 1)) {
-          s_err = 1;
-          break;
+      uint32_t g = 0;  // k-blocks issued so far
+      for (int tile = blockIdx.x; tile < n_tiles && !*err; tile += gridDim.x) {
+        const int mt = tile % m_tiles, vt = tile / m_tiles;
+        const bool pair = mt < P.n_pair_tiles;
+        const int row0 = pair ? mt * kBM : P.n_pair_rows + (mt - P.n_pair_tiles) * kBM;
+        const uint32_t bytes = pair ? kStageBytes : (kTileA + kTileB);  // target-only tiles: A_t and B_t
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+          const int s = static_cast<int>(g % kLStages);
+          if (g >= static_cast<uint32_t>(kLStages) &&
+              !mbar_wait_bounded(&empty_bar[s], ((g / kLStages) - 1) & 1)) {
+            *err = 1;
+            break;
+          }
+          uint8_t* st = ring + s * kStageBytes;
+          mbar_arrive_expect_tx(&full_bar[s], bytes);
+          const int x = kb * kBK;
+          if (pair) {
+            tma_load_2d(st, &map_hd, x, row0, &full_bar[s]);
+            if (!kShared) tma_load_2d(st + RG::kOffBz, &map_wd, x, vt * kBN, &full_bar[s]);
+          }
+          tma_load_2d(st + kTileA, &map_ht, x, row0, &full_bar[s]);
+          tma_load_2d(st + RG::kOffBt, &map_wt, x, vt * kBN, &full_bar[s]);
         }
-        uint8_t* st = ring + s * kStageBytes;
-        mbar_arrive_expect_tx(&full_bar[s], bytes);
-        const int x = kb * kBK;
-        if (pair) {
-          tma_load_2d(st, &map_hd, x, row0, &full_bar[s]);
-          tma_load_2d(st + 2 * kTileA, &map_wd, x, v0, &full_bar[s]);
-        }
-        tma_load_2d(st + kTileA, &map_ht, x, row0, &full_bar[s]);
-        tma_load_2d(st + 2 * kTileA + kTileB, &map_wt, x, v0, &full_bar[s]);
       }
     }
     __syncwarp();
@@ -122,161 +189,176 @@ __global__ void __launch_bounds__(kLThreads, 1)
     // ---- MMA issuer ----
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kLStages;
-        if (!mbar_wait_bounded(&full_bar[s], (kb / kLStages) & 1)) {
-          s_err = 1;
+      uint32_t g = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < n_tiles && !*err; tile += gridDim.x, ++it) {
+        const bool pair = (tile % m_tiles) < P.n_pair_tiles;
+        // the epilogue has read the previous tile's accumulators
+        if (it > 0 && !mbar_wait_bounded(&accum_empty, (it - 1) & 1)) {
+          *err = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t st = smem_addr(ring + s * kStageBytes);
-        const uint64_t daz = sdesc_sw128(st), dat = sdesc_sw128(st + kTileA);
-        const uint64_t dbz = sdesc_sw128(st + 2 * kTileA), dbt = sdesc_sw128(st + 2 * kTileA + kTileB);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+          const int s = static_cast<int>(g % kLStages);
+          if (!mbar_wait_bounded(&full_bar[s], (g / kLStages) & 1)) {
+            *err = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_addr(ring + s * kStageBytes);
+          const uint64_t daz = sdesc_swizzled<kRowBytes>(st), dat = sdesc_swizzled<kRowBytes>(st + kTileA);
+          const uint64_t dbz = sdesc_swizzled<kRowBytes>(st + RG::kOffBz);
+          const uint64_t dbt = sdesc_swizzled<kRowBytes>(st + RG::kOffBt);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-          const uint64_t step = static_cast<uint64_t>(kk * 2);  // 32 bytes per 16-element step, in 16-byte units
-          if (pair) umma_bf16(tmem, daz + step, dbz + step, idesc, acc);
-          umma_bf16(tmem + kBN, dat + step, dbt + step, idesc, acc);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            const uint64_t step = static_cast<uint64_t>(kk * 2);  // 32 bytes per 16-element step, in 16-byte units
+            if (pair) umma_bf16(tmem, daz + step, dbz + step, idesc, acc);
+            umma_bf16(tmem + kBN, dat + step, dbt + step, idesc, acc);
+          }
+          umma_commit(&empty_bar[s]);
         }
-        umma_commit(&empty_bar[s]);
+        umma_commit(&accum_full);  // arrives once every MMA issued so far has completed
+        if (!ok) break;
       }
-      umma_commit(&accum_bar);  // arrives once every MMA issued above has completed
     }
     __syncwarp();
   } else {
-    // ---- epilogue: warp w reads TMEM lanes 32 (w mod 4) .. +31 ----
-    const int q = warp & 3;
-    const int r = q * 32 + lane;  // row of the tile
-    const int row = row0 + r;
-    const bool valid_row = row < row_end;
-    const bool ok = mbar_wait_bounded(&accum_bar, 0);
-    tc_fence_after();
-    if (!ok) s_err = 1;
+    // ---- epilogue ----
+    const int q = warp & 3;              // TMEM lane quarter
+    const int j = (warp - 2) >> 2;       // column quarter: 64 j .. 64 j + 63
+    const int r = q * 32 + lane;         // row of the tile
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    if (P.mode == 1) {
-      // diagnostic: write the logits tiles
-      for (int c = 0; c < kBN / 16; ++c) {
-        uint32_t rt[16];
-        tmem_ld16(tl + kBN + c * 16, rt);
+    int it = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+      const int mt = tile % m_tiles, vt = tile / m_tiles;
+      const bool pair = mt < P.n_pair_tiles;
+      const int row0 = pair ? mt * kBM : P.n_pair_rows + (mt - P.n_pair_tiles) * kBM;
+      const int row = row0 + r;
+      const bool valid_row = row < (pair ? P.n_pair_rows : P.n_t_rows);
+      // every epilogue warp runs every tile and every barrier below, whatever the
+      // waits return, so the named barriers always see all sixteen warps
+      const bool ok = !*err && mbar_wait_bounded(&accum_full, it & 1);
+      tc_fence_after();
+      if (!ok) *err = 1;
+      EpiRec e{kNegInf, 0.f, 0.f, kNegInf, kNegInf, kNegInf, 0.f, 0.f, -1, -1};
+      for (int c = 0; c < 4; ++c) {
+        const int col = j * 64 + c * 16;
+        uint32_t rt[16], rz[16];
+        tmem_ld16(tl + kBN + col, rt);
         tmem_wait16(rt);
-        if (ok && valid_row) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int v = v0 + c * 16 + j;
-            if (v < P.V) P.out_t[static_cast<int64_t>(row) * P.ld_out + v] = __uint_as_float(rt[j]);
-          }
-        }
         if (pair) {
-          uint32_t rz[16];
-          tmem_ld16(tl + c * 16, rz);
+          tmem_ld16(tl + col, rz);
           tmem_wait16(rz);
+        }
+        const int vb = vt * kBN + col;
+        const int nval = min(16, P.V - vb);  // entries of this chunk inside the vocabulary
+        if (P.mode == 1) {
           if (ok && valid_row) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int v = v0 + c * 16 + j;
-              if (v < P.V) P.out_z[static_cast<int64_t>(row) * P.ld_out + v] = __uint_as_float(rz[j]);
+            for (int x = 0; x < 16; ++x) {
+              if (x < nval) {
+                P.out_t[static_cast<int64_t>(row) * P.ld_out + vb + x] = __uint_as_float(rt[x]);
+                if (pair) P.out_z[static_cast<int64_t>(row) * P.ld_out + vb + x] = __uint_as_float(rz[x]);
+              }
             }
           }
+          continue;
         }
-      }
-    } else {
-      // statistics of this row over the tile's valid entries (natural exponentials
-      // as 2^(x log2 e), every sum relative to the running maximum)
-      float mz = kNegInf, sz = 0.f, szd = 0.f, dmax = kNegInf, z2 = kNegInf;
-      float mt = kNegInf, st = 0.f, zat = 0.f;
-      int az = -1, at = -1;
-      for (int c = 0; c < kBN / 16; ++c) {
-        uint32_t rt[16], rz[16];
-        tmem_ld16(tl + kBN + c * 16, rt);
-        tmem_wait16(rt);
-        if (pair) {
-          tmem_ld16(tl + c * 16, rz);
-          tmem_wait16(rz);
-        }
-        const int vb = v0 + c * 16;
-        const int nval = min(16, P.V - vb);  // entries of this chunk inside the vocabulary
         if (nval <= 0) continue;
         // t: maximum with its first index (and z there), then the rescaled sum
         float cmt = kNegInf, czat = 0.f;
         int cat = -1;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float t = __uint_as_float(rt[j]);
-          if (j < nval && t > cmt) {
+        for (int x = 0; x < 16; ++x) {
+          const float t = __uint_as_float(rt[x]);
+          if (x < nval && t > cmt) {
             cmt = t;
-            cat = vb + j;
-            if (pair) czat = __uint_as_float(rz[j]);
+            cat = vb + x;
+            if (pair) czat = __uint_as_float(rz[x]);
           }
         }
-        if (cmt > mt) {
-          st *= ex2((mt - cmt) * kLog2e);
-          mt = cmt;
-          at = cat;
-          zat = czat;
+        if (cmt > e.mt) {
+          e.st *= ex2((e.mt - cmt) * kLog2e);
+          e.mt = cmt;
+          e.at = cat;
+          e.zat = czat;
         }
         float add_t = 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (j < nval) add_t += ex2((__uint_as_float(rt[j]) - mt) * kLog2e);
-        st += add_t;
+        for (int x = 0; x < 16; ++x)
+          if (x < nval) add_t += ex2((__uint_as_float(rt[x]) - e.mt) * kLog2e);
+        e.st += add_t;
         if (pair) {
           // z: the two largest values (first index of the largest), max (z - t)
           float c1 = kNegInf, c2 = kNegInf;
           int ci = -1;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float z = __uint_as_float(rz[j]);
-            if (j < nval) {
+          for (int x = 0; x < 16; ++x) {
+            const float z = __uint_as_float(rz[x]);
+            if (x < nval) {
               if (z > c1) {
                 c2 = c1;
                 c1 = z;
-                ci = vb + j;
+                ci = vb + x;
               } else if (z > c2) {
                 c2 = z;
               }
-              dmax = fmaxf(dmax, z - __uint_as_float(rt[j]));
+              e.dmax = fmaxf(e.dmax, z - __uint_as_float(rt[x]));
             }
           }
-          if (c1 > mz) {
-            const float f = ex2((mz - c1) * kLog2e);
-            sz *= f;
-            szd *= f;
-            z2 = fmaxf(mz, c2);
-            mz = c1;
-            az = ci;
+          if (c1 > e.mz) {
+            const float f = ex2((e.mz - c1) * kLog2e);
+            e.sz *= f;
+            e.szd *= f;
+            e.z2 = fmaxf(e.mz, c2);
+            e.mz = c1;
+            e.az = ci;
           } else {
-            z2 = fmaxf(z2, c1);
+            e.z2 = fmaxf(e.z2, c1);
           }
           float add_z = 0.f, add_zd = 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (j < nval) {
-              const float z = __uint_as_float(rz[j]);
-              const float e = ex2((z - mz) * kLog2e);
-              add_z += e;
-              add_zd = fmaf(e, z - __uint_as_float(rt[j]), add_zd);
+          for (int x = 0; x < 16; ++x) {
+            if (x < nval) {
+              const float z = __uint_as_float(rz[x]);
+              const float ez = ex2((z - e.mz) * kLog2e);
+              add_z += ez;
+              add_zd = fmaf(ez, z - __uint_as_float(rt[x]), add_zd);
             }
           }
-          sz += add_z;
-          szd += add_zd;
+          e.sz += add_z;
+          e.szd += add_zd;
         }
       }
-      if (ok && valid_row) {
+      // the accumulators are read: the next tile's MMAs may start
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accum_empty);
+      if (P.mode == 1) continue;
+      red[j * kBM + r] = e;
+      named_bar_sync_id(1, kEpiWarps * 32);
+      if (j == 0 && ok && valid_row) {
+        EpiRec m = red[r];
+        for (int jj = 1; jj < 4; ++jj) epi_merge(m, red[jj * kBM + r]);
         LmPartial rec;
-        rec.mz = mz;
-        rec.sz = sz;
-        rec.szd = szd;
-        rec.dmax = dmax;
-        rec.z2 = z2;
-        rec.mt = mt;
-        rec.st = st;
-        rec.az = az;
-        rec.at = at;
-        rec.zat = zat;
+        rec.mz = m.mz;
+        rec.sz = m.sz;
+        rec.szd = m.szd;
+        rec.dmax = m.dmax;
+        rec.z2 = m.z2;
+        rec.mt = m.mt;
+        rec.st = m.st;
+        rec.az = m.az;
+        rec.at = m.at;
+        rec.zat = m.zat;
         rec.pad1 = rec.pad2 = 0;
         P.partials[static_cast<int64_t>(row) * P.n_vtiles + vt] = rec;
       }
+      named_bar_sync_id(1, kEpiWarps * 32);  // red is rewritten by the next tile
     }
   }
   tc_fence_before();
@@ -570,7 +652,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 matrix [rows, cols] with row stride ld elements, tiles of box_rows x 64 (128-byte swizzle).
+// bf16 matrix [rows, cols] with row stride ld elements, tiles of box_rows x kBK (swizzled at kBK * 2 bytes).
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -579,7 +661,8 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int6
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, kRowBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -611,13 +694,20 @@ cudaError_t launch_lm_gemm(const uint16_t* hd, int64_t ld_hd, const uint16_t* ht
     mhd = mht;
     mwd = mwt;
   }
-  const size_t smem = static_cast<size_t>(kLStages) * kStageBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(lmhead_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  const bool shared = (wd == wt) && (ld_wd == ld_wt);
+  const size_t smem = (shared ? static_cast<size_t>(Ring<true>::kStages) * Ring<true>::kStage
+                              : static_cast<size_t>(Ring<false>::kStages) * Ring<false>::kStage) +
+                      4 * kBM * sizeof(EpiRec) + 1024;
+  auto kern = shared ? lmhead_gemm_kernel<true> : lmhead_gemm_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  const long long tiles = static_cast<long long>(m_tiles) * p.n_vtiles;
+  const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);  // one CTA per SM (shared memory)
   count_launch();
-  lmhead_gemm_kernel<<<dim3(static_cast<unsigned>(m_tiles), static_cast<unsigned>(p.n_vtiles)), kLThreads, smem, s>>>(
-      mhd, mht, mwd, mwt, p);
+  kern<<<grid, kGemmThreads, smem, s>>>(mhd, mht, mwd, mwt, p);
   return cudaGetLastError();
 }
 

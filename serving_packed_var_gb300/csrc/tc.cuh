@@ -14,7 +14,8 @@
 // A K-major tile of R rows x 64 bf16 loaded by TMA with 128-byte swizzling is R
 // rows of 128 bytes, the 16-byte chunks of row r permuted by r mod 8; groups of 8
 // rows are 1024 bytes apart (the stride byte offset), and the 16-element step of
-// one MMA along K advances the start address by 32 bytes.
+// one MMA along K advances the start address by 32 bytes.  With 32 bf16 per row and
+// 64-byte swizzling the rows are 64 bytes and the groups 512 bytes apart.
 #pragma once
 
 #include <cstdint>
@@ -50,12 +51,16 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+// K-major tile of rows of `row_bytes` (128 or 64) swizzled at that width: 8-row groups
+// are 8 * row_bytes apart; swizzle mode 2 (128-byte) or 4 (64-byte).
+template <int kRowBytes>
+__device__ __forceinline__ uint64_t sdesc_swizzled(uint32_t saddr) {
+  static_assert(kRowBytes == 128 || kRowBytes == 64, "128- or 64-byte swizzle");
   uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1) << 16;          // leading byte offset (unused with 128-byte swizzle)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;  // stride byte offset: 8 rows of 128 bytes
-  d |= static_cast<uint64_t>(1) << 46;          // fixed value
-  d |= static_cast<uint64_t>(2) << 61;          // 128-byte swizzle
+  d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused when swizzled)
+  d |= static_cast<uint64_t>((8 * kRowBytes) >> 4) << 32;  // stride byte offset: 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                   // fixed value
+  d |= static_cast<uint64_t>(kRowBytes == 128 ? 2 : 4) << 61;
   return d;
 }
 
