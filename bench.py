@@ -31,6 +31,8 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 SAMPLED_T = 0.8  # temperature of the sampled-verification measurement
+LMHEAD_HIDDEN = 4096  # Qwen3-8B hidden size for the logit-free measurement
+LMHEAD_CALLS = 10
 
 
 # Sources that decide each kernel's code; a recorded ncu figure is used only while they are unchanged.
@@ -336,6 +338,10 @@ def run_ours(args):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
 
+    # the logit-free forward from hidden states at Qwen3-8B shapes (H = 4096, shared head),
+    # the same packed layout as this workload
+    lm = run_lmhead(args, w, dev, af, torch, np, stream)
+
     # end to end: pinned host inputs -> device, step, verify outputs + loss back to host
     e2e = run_e2e(args, b, w, dev, af, torch, np)
 
@@ -377,6 +383,19 @@ def run_ours(args):
                 "kernel": kernels[dom]["kernels"], "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": kernels[dom]["bytes"]}
+    roofline_lmhead = None
+    if lm is not None:
+        tpeak, tkind = tensor_peak()
+        kernels["lmhead_fwd"] = {"kernels": "L0 gather + L1 tcgen05 head GEMM with per-tile row reduction + "
+                                            "L2 combine + K2 (adaflash_lmhead_opd_fwd), calls back to back",
+                                 "ms": lm["ms"], "flops": lm["flops"], "achieved_tflops": lm["tflops"],
+                                 "frac": lm["tflops"] / tpeak, "rows_per_s": Nd / (lm["ms"] * 1e-3),
+                                 "hidden": lm["hidden"], "vocab": lm["vocab"]}
+        roofline_lmhead = {"bound": "tensor", "achieved": lm["tflops"], "peak": tpeak, "unit": "TFLOP/s",
+                           "frac": lm["tflops"] / tpeak, "traffic": None,
+                           "kernel": "logit-free verify + loss forward (head GEMM dominant)",
+                           "algorithmic_flops_per_launch": lm["flops"],
+                           "peak_source": f"{tkind} (MEASURED_PEAKS.json bf16_tflops, burst)"}
     roofline_fwd = {"bound": "hbm", "achieved": fwd_alone_gbs, "peak": peak, "unit": "GB/s",
                     "frac": fwd_alone_gbs / peak,
                     "traffic": traffic.get("rowpass_kernel", {}).get("dram_bytes_per_launch"),
@@ -387,7 +406,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; no datasets or weights)",
-        "config": workload_config(w), "roofline": roofline, "roofline_fwd": roofline_fwd, "kernels": kernels,
+        "config": workload_config(w), "roofline": roofline, "roofline_fwd": roofline_fwd,
+        "roofline_lmhead": roofline_lmhead, "kernels": kernels,
         "e2e": e2e, "gpu_launches": launches, "clocks": clk.summary(),
         "cpu_baseline": cpu_baseline(b) if world == 1 or rank == 0 else None,
         "impl": "ours",
@@ -396,6 +416,54 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_lmhead(args, w, dev, af, torch, np, stream):
+    """Time adaflash_lmhead_opd_fwd on hidden states of this workload's packed layout."""
+    if args.no_lmhead:
+        return None
+    from synth.lmhead import LMHeadWorkload, materialize_lmhead
+    lw = LMHeadWorkload(name="lm_" + w.name, vocab=w.vocab, hidden=LMHEAD_HIDDEN, k=w.k,
+                        planted_accept=w.planted_accept, clip_c=w.clip_c, ce_weight=w.ce_weight, seed=w.seed)
+    lb = materialize_lmhead(lw)
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    hd, ht, wh = dev_bf16(lb.hd), dev_bf16(lb.ht), dev_bf16(lb.wt)
+    tok = torch.from_numpy(lb.tokens).to(dev)
+    doff = torch.from_numpy(lb.doff).to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    R, Nd = lw.num_requests, lw.num_draft_rows
+    ws = torch.empty(af.adaflash_lmhead_workspace_bytes(R, Nd, lw.vocab, lw.hidden), dtype=torch.uint8, device=dev)
+    out = af.adaflash_lmhead_opd_fwd(hd, ht, wh, wh, tok, doff, lw.clip_c, lw.ce_weight, workspace=ws, status=st)
+    for _ in range(2):
+        af.adaflash_lmhead_opd_fwd(hd, ht, wh, wh, tok, doff, lw.clip_c, lw.ce_weight, workspace=ws, out=out,
+                                   status=st)
+    torch.cuda.synchronize()
+    n = LMHEAD_CALLS
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        af.adaflash_lmhead_opd_fwd(hd, ht, wh, wh, tok, doff, lw.clip_c, lw.ce_weight, workspace=ws, out=out,
+                                   status=st)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())} (lmhead)")
+    ms = a.elapsed_time(b) / n
+    flops = 2.0 * (2 * Nd + R) * lw.hidden * lw.vocab
+    del hd, ht, wh, ws
+    return {"ms": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12, "hidden": lw.hidden, "vocab": lw.vocab}
 
 
 def run_e2e(args, b, w, dev, af, torch, np):
@@ -486,6 +554,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c128")
+    ap.add_argument("--no-lmhead", action="store_true", help="skip the logit-free (hidden-state) measurement")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
