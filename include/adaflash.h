@@ -255,6 +255,42 @@ adaflash_status adaflash_lmhead_opd_fwd(
     uint32_t* d_status, void* stream);
 
 /*
+ * adaflash_lmhead_opd_fwd_static -- adaflash_lmhead_opd_fwd without a workspace argument.
+ *
+ * The pages have no counterpart: this entry point is for callers that cannot hand
+ * the library device memory.  A plugin called by a host framework that owns every
+ * allocation (an inference server's custom-op slot, a runtime with its own pooled
+ * allocator) may have no way to call cudaMalloc, or may be forbidden to because an
+ * allocation would synchronise the device or break the framework's memory
+ * accounting.  Such a caller passes only its inputs and outputs; the scratch the
+ * logit-free forward needs (the gathered hidden rows and the per-tile records) lives
+ * in one static device array of ADAFLASH_LMHEAD_STATIC_SCRATCH_BYTES inside this
+ * library, which every GPU that loads the library's LM-head code holds until the
+ * process exits.
+ *
+ * Arguments, outputs and results are those of adaflash_lmhead_opd_fwd.  A batch whose
+ * adaflash_lmhead_workspace_bytes(R, N_d, V, H) exceeds the array is rejected with
+ * ADAFLASH_ERR_UNSUPPORTED before anything is enqueued.  The first call on a device
+ * looks up the array's device address with that device current (set-up done once
+ * per device); make that first call before any stream capture.  Nothing here calls
+ * cudaMalloc or cudaFree.  All calls share the one array and each leaves its contents
+ * behind: a call writes every scratch byte it reads before reading it, so nothing is
+ * cleared, but calls whose kernels overlap on the GPU (other streams, other host
+ * threads) race on the array and must be serialised by the caller.
+ */
+#define ADAFLASH_LMHEAD_STATIC_SCRATCH_BYTES (48ll << 20)
+
+adaflash_status adaflash_lmhead_opd_fwd_static(
+    const void* draft_hidden, int64_t ld_hd, const void* target_hidden, int64_t ld_ht,
+    const void* draft_head, int64_t ld_wd, const void* target_head, int64_t ld_wt, int32_t hidden,
+    const int32_t* draft_tokens, const int32_t* draft_offsets,
+    int32_t num_requests, int32_t num_draft_rows, int32_t vocab,
+    float clip_c, float ce_weight,
+    int32_t* target_argmax, int32_t* accept_len, int32_t* bonus_token, float* accept_rate,
+    float* kl_row, float* ce_row, float* row_stats, float* loss,
+    uint32_t* d_status, void* stream);
+
+/*
  * Variable-length request packing with an EMA capacity estimate (host side).
  *
  * The AdaFlash article ("Infrastructure: Async Training & Variable-Length Batching",

@@ -47,6 +47,8 @@ SIGNATURES = {
     "adaflash_lmhead_logits": [_vp, _i64, _i32, _vp, _i64, _i32, _i32, _vp, _i64, _vp, _vp],
     "adaflash_lmhead_opd_fwd": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _i32, _i32, _i32,
                                 _f32, _f32, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "adaflash_lmhead_opd_fwd_static": [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _i32, _i32, _i32,
+                                       _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "adaflash_packer_create": [_i32, _f64, _f64, _vp],
     "adaflash_packer_destroy": [_vp],
     "adaflash_packer_plan": [_vp, _vp, _i32, _vp, _vp, _vp, _vp],

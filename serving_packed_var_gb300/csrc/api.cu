@@ -513,6 +513,28 @@ adaflash_status adaflash_lmhead_opd_fwd(const void* draft_hidden, int64_t ld_hd,
   return ADAFLASH_OK;
 }
 
+adaflash_status adaflash_lmhead_opd_fwd_static(const void* draft_hidden, int64_t ld_hd, const void* target_hidden,
+                                               int64_t ld_ht, const void* draft_head, int64_t ld_wd,
+                                               const void* target_head, int64_t ld_wt, int32_t hidden,
+                                               const int32_t* draft_tokens, const int32_t* draft_offsets,
+                                               int32_t num_requests, int32_t num_draft_rows, int32_t vocab,
+                                               float clip_c, float ce_weight, int32_t* target_argmax,
+                                               int32_t* accept_len, int32_t* bonus_token, float* accept_rate,
+                                               float* kl_row, float* ce_row, float* row_stats, float* loss,
+                                               uint32_t* d_status, void* stream) {
+  const int64_t need = adaflash_lmhead_workspace_bytes(num_requests, num_draft_rows, vocab, hidden);
+  if (need < 0) return ADAFLASH_ERR_INVALID_ARG;
+  if (need > ADAFLASH_LMHEAD_STATIC_SCRATCH_BYTES) return ADAFLASH_ERR_UNSUPPORTED;
+  ADAFLASH_TRY(check_device());
+  void* scratch = nullptr;
+  int64_t bytes = 0;
+  ADAFLASH_CUDA(lm_static_scratch(&scratch, &bytes));
+  return adaflash_lmhead_opd_fwd(draft_hidden, ld_hd, target_hidden, ld_ht, draft_head, ld_wd, target_head, ld_wt,
+                                 hidden, draft_tokens, draft_offsets, num_requests, num_draft_rows, vocab, clip_c,
+                                 ce_weight, scratch, bytes, target_argmax, accept_len, bonus_token, accept_rate,
+                                 kl_row, ce_row, row_stats, loss, d_status, stream);
+}
+
 adaflash_status adaflash_verify_sampled(const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
                                         const void* target_logits, adaflash_dtype t_dtype, int64_t ld_t,
                                         const int32_t* draft_tokens, const int32_t* draft_offsets,

@@ -146,6 +146,8 @@ cudaError_t launch_lm_gemm(const uint16_t* hd, int64_t ld_hd, const uint16_t* ht
                            const uint16_t* wd, int64_t ld_wd, const uint16_t* wt, int64_t ld_wt,
                            const LmHeadParams& p, cudaStream_t s);
 cudaError_t launch_lm_combine(const LmCombineParams& p, cudaStream_t s);
+// Device address (looked up once per device) and size of the static scratch array.
+cudaError_t lm_static_scratch(void** ptr, int64_t* bytes);
 cudaError_t launch_sampled(const SampledParams& p, int z_dtype, int t_dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_selftest_wait(uint32_t* status, int32_t limit_us, cudaStream_t s);
 

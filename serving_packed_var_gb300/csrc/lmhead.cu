@@ -21,6 +21,7 @@
 //      exceed the clip, and writes the outputs of the logits path (kl, ce, row
 //      statistics, target argmax).
 // A diagnostic entry point runs L1 with an epilogue that writes the logits instead.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 #include <cmath>
@@ -667,6 +668,28 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int6
 }
 
 }  // namespace
+
+// The scratch of adaflash_lmhead_opd_fwd_static: one array per device, held while the
+// library's LM-head code is loaded.  Host code cannot use the symbol as a device
+// address; lm_static_scratch looks the address up once per device.
+static __device__ __align__(256) uint8_t g_lm_static_scratch[ADAFLASH_LMHEAD_STATIC_SCRATCH_BYTES];
+
+cudaError_t lm_static_scratch(void** ptr, int64_t* bytes) {
+  static std::atomic<void*> cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    e = cudaGetSymbolAddress(&p, g_lm_static_scratch);  // with this device current
+    if (e != cudaSuccess) return e;
+    cache[dev].store(p, std::memory_order_release);
+  }
+  *ptr = p;
+  *bytes = ADAFLASH_LMHEAD_STATIC_SCRATCH_BYTES;
+  return cudaSuccess;
+}
 
 cudaError_t launch_lm_gather(const uint16_t* ht, int64_t ld_ht, const int32_t* doff, int R, int N_d, int H,
                              uint16_t* out, uint32_t* status, cudaStream_t s) {
