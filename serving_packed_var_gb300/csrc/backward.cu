@@ -15,6 +15,10 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#ifndef ADAFLASH_BWD_REVERSE
+#define ADAFLASH_BWD_REVERSE 1
+#endif
+
 namespace adaflash {
 
 namespace {
@@ -64,7 +68,13 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams P) {
   __shared__ RowCoef s_coef;
   __shared__ int s_ok;
   __shared__ int s_trow;
+#if ADAFLASH_BWD_REVERSE
+  // rows in reverse order: the forward's last rows, and the rows the next forward reads
+  // first, are the ones still in L2
+  const int d = P.N_d - 1 - static_cast<int>(blockIdx.x) / P.chunks_per_row;
+#else
   const int d = static_cast<int>(blockIdx.x) / P.chunks_per_row;
+#endif
   const int chunk = static_cast<int>(blockIdx.x) % P.chunks_per_row;
 
   if (threadIdx.x == 0) {
