@@ -59,6 +59,8 @@ constexpr uint32_t kTileA = kBM * kBK * 2;
 constexpr uint32_t kTileB = kBN * kBK * 2;
 constexpr uint32_t kTmemCols = 512;  // z tile in columns 0..255, t tile in 256..511
 constexpr int kCombThreads = 256;
+constexpr int kMaxVTiles = (ADAFLASH_MAX_VOCAB + 255) / 256;  // vocabulary tiles of a row, at most
+constexpr int kWin = 512;                                      // candidate entries per evaluation window
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -461,9 +463,12 @@ __device__ __forceinline__ void racc_merge(RowAcc& a, const RowAcc& b) {
 // ---- L2: per-row combine, exact re-evaluation of clip candidates, outputs ----
 __global__ void __launch_bounds__(kCombThreads) lm_combine_kernel(const LmCombineParams P) {
   __shared__ RowAcc red[kCombThreads];
-  __shared__ int s_cand[kCombThreads];  // entries of the current batch
-  __shared__ float s_corr[kCombThreads], s_sclip[kCombThreads];
-  __shared__ int s_nclip[kCombThreads];
+  __shared__ int s_off[kMaxVTiles];  // candidate entries per tile, then their first list position
+  __shared__ int s_wsum[kCombThreads / 32];
+  __shared__ int s_total;
+  __shared__ int s_list[kWin];  // vocabulary entries of the current window
+  __shared__ float s_corr[kWin], s_sclip[kWin];
+  __shared__ int s_flag[kWin];
   __shared__ float s_lse_z, s_lse_t, s_dlse, s_klu, s_theta, s_za;
   __shared__ int s_a, s_ok, s_d, s_s;
   const int r = static_cast<int>(blockIdx.x);
@@ -545,44 +550,64 @@ __global__ void __launch_bounds__(kCombThreads) lm_combine_kernel(const LmCombin
   // ---- exact terms of the entries that can exceed the clip ----
   // A tile is a candidate when its largest z clears theta; only its largest entry
   // can then clip unless its second largest z clears theta too, when every entry of
-  // the tile is examined.  Entries are taken in vocabulary order, in batches.
+  // the tile is examined.  The candidate count of every tile is found in parallel, a
+  // block scan in tile order places the entries, and windows of kWin entries are
+  // evaluated (one warp per entry) and summed in vocabulary order.
   const float theta = s_theta;
   const float lse_z = s_lse_z, dlse = s_dlse, c = P.clip_c;
   const float nlz = -lse_z * kLog2e;
+  const int nt = P.n_vtiles;  // <= kMaxVTiles
+  for (int v = tid; v < nt; v += kCombThreads) {
+    const LmPartial p = rec[v];
+    s_off[v] = !(p.mz > theta) ? 0 : (!(p.z2 > theta) ? 1 : min(256, P.V - v * 256));
+  }
+  __syncthreads();
+  // exclusive scan of s_off over tiles: thread t owns tiles [t * per, (t + 1) * per)
+  {
+    const int per = (nt + kCombThreads - 1) / kCombThreads;
+    const int t0 = min(nt, tid * per), t1 = min(nt, t0 + per);
+    int mine = 0;
+    for (int v = t0; v < t1; ++v) mine += s_off[v];
+    int inc = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += y;
+    }
+    if (lane == 31) s_wsum[warp] = inc;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < kCombThreads / 32; ++w) {
+      if (w < warp) before += s_wsum[w];
+      total += s_wsum[w];
+    }
+    int run = before + inc - mine;
+    for (int v = t0; v < t1; ++v) {
+      const int cnt = s_off[v];
+      s_off[v] = run;  // first list position of tile v
+      run += cnt;
+    }
+    if (tid == 0) s_total = total;
+  }
+  __syncthreads();
+  const int total = s_total;
   float corr_all = 0.f, sclip_all = 0.f;
   int nclip_all = 0;
-  int vt = 0, sub = 0;  // scan position (thread 0)
-  while (true) {
-    __syncthreads();
-    if (tid == 0) {
-      int n = 0;
-      while (vt < P.n_vtiles && n < kCombThreads) {
-        const LmPartial p = rec[vt];
-        if (!(p.mz > theta)) {
-          ++vt;
-          continue;
-        }
-        if (!(p.z2 > theta)) {
-          s_cand[n++] = p.az;
-          ++vt;
-          continue;
-        }
-        const int v0 = vt * 256;
-        const int vend = min(P.V, v0 + 256);
-        while (v0 + sub < vend && n < kCombThreads) s_cand[n++] = v0 + sub++;
-        if (v0 + sub >= vend) {
-          sub = 0;
-          ++vt;
-        }
+  for (int lo = 0; lo < total; lo += kWin) {
+    const int hi = min(total, lo + kWin);
+    // place the entries of this window
+    for (int v = tid; v < nt; v += kCombThreads) {
+      const int o0 = s_off[v], o1 = (v + 1 < nt) ? s_off[v + 1] : total;
+      if (o1 <= lo || o0 >= hi) continue;
+      if (o1 - o0 == 1) {
+        s_list[o0 - lo] = rec[v].az;
+      } else {
+        for (int x = max(o0, lo); x < min(o1, hi); ++x) s_list[x - lo] = v * 256 + (x - o0);
       }
-      s_nclip[0] = n;  // batch size
     }
     __syncthreads();
-    const int n = s_nclip[0];
-    if (n == 0) break;
-    __syncthreads();
-    for (int e = warp; e < n; e += kCombThreads / 32) {
-      const int v = s_cand[e];
+    for (int e = warp; e < hi - lo; e += kCombThreads / 32) {
+      const int v = s_list[e];
       float corr = 0.f, sc = 0.f;
       int nc = 0;
       if (v >= 0 && v < P.V) {
@@ -602,17 +627,18 @@ __global__ void __launch_bounds__(kCombThreads) lm_combine_kernel(const LmCombin
       if (lane == 0) {
         s_corr[e] = corr;
         s_sclip[e] = sc;
-        s_cand[e] = nc;  // reused: this entry's clip flag
+        s_flag[e] = nc;
       }
     }
     __syncthreads();
     if (tid == 0) {
-      for (int e = 0; e < n; ++e) {
+      for (int e = 0; e < hi - lo; ++e) {
         corr_all += s_corr[e];
         sclip_all += s_sclip[e];
-        nclip_all += s_cand[e];
+        nclip_all += s_flag[e];
       }
     }
+    __syncthreads();
   }
   if (tid == 0) {
     P.kl_row[d] = s_klu - corr_all;
