@@ -433,6 +433,9 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
 // host side
 // ---------------------------------------------------------------------------
 
+#ifndef ADAFLASH_ROWPASS_TAIL
+#define ADAFLASH_ROWPASS_TAIL 1  // the last partial wave of units as a second launch with larger clusters
+#endif
 #ifndef ADAFLASH_ROWPASS_SLICE_TARGET
 #define ADAFLASH_ROWPASS_SLICE_TARGET 160000
 #endif
@@ -567,7 +570,8 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   p.wait_prior = 0;
   const int clusters = active_clusters<DZ, DT, kFast>(p.cluster, rowpass_smem<DZ, DT, kFast>(p.slice));
   const int split = (units / clusters) * clusters;
-  if (units <= clusters || split == units || p.cluster >= kMaxCluster) return launch_range<DZ, DT, kFast>(p, false, stream);
+  if (!ADAFLASH_ROWPASS_TAIL || units <= clusters || split == units || p.cluster >= kMaxCluster)
+    return launch_range<DZ, DT, kFast>(p, false, stream);
   RowPassParams tail = p;
   p.unit_end = split;
   cudaError_t e = launch_range<DZ, DT, kFast>(p, false, stream);

@@ -150,6 +150,38 @@ def test_edge_shapes(case):
     _check(b, h, range(b.w.num_draft_rows))
 
 
+def test_padded_rows_and_strided_views():
+    # every matrix a view with ld > H (rows still 16-byte aligned), separate heads
+    import serving_packed_var_gb300 as af
+    b = materialize_lmhead(custom_lmhead(vocab=1500, hidden=256, k=[5, 16, 2], shared_head=False))
+    w = b.w
+
+    def padded(bits, extra):
+        n, H = bits.shape
+        full = np.zeros((n, H + extra), dtype=np.uint16)
+        full[:, :H] = bits
+        return _dev_bf16(full)[:, :H]
+
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hd, ht, wd, wt = padded(b.hd, 8), padded(b.ht, 64), padded(b.wd, 24), padded(b.wt, 8)
+    assert hd.stride(0) == 264 and ht.stride(0) == 320
+    out = af.adaflash_lmhead_opd_fwd(hd, ht, wd, wt, torch.from_numpy(b.tokens).cuda(), torch.from_numpy(b.doff).cuda(),
+                                     w.clip_c, w.ce_weight, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    h = {k: v.cpu().numpy() for k, v in out.items()}
+    _check_verify(b, h)
+    _check(b, h, range(w.num_draft_rows))
+
+
+def test_single_request_qwen3_8b_shapes():
+    b = materialize_lmhead(custom_lmhead(vocab=151936, hidden=4096, k=[16], spike=18.0))
+    h, st = _run(b)
+    assert st == 0
+    _check_verify(b, h)
+    _check(b, h, [0, 9, 15])
+
+
 def test_qwen3_8b_shapes_c32_sampled_rows():
     b = materialize_lmhead(make_lmhead_workload("lm_c32"))
     h, st = _run(b)
