@@ -470,64 +470,70 @@ __global__ void __launch_bounds__(kDrawThreads, ADAFLASH_DRAW_MINBLOCKS) sampled
         if (cown[r] >= 0) orank = r;
       if (orank < 0) {
         if (rank == 0 && tid == 0) P.next_token[i] = -1;  // no mass at all (non-finite logits)
-      } else if (rank == orank && warp == cown[orank]) {
-        // stage the segment's weights (coalesced), then walk it tile by tile: lane sums
-        // of 8 entries, a warp scan, and the first lane whose running sum passes the
-        // threshold resolves within its 8 entries
-        const int ntiles = (s1 - s0 + 255) >> 8;
-        for (int t = 0; t < ntiles; ++t) {
+      } else if (rank == orank) {
+        // every warp of the owner CTA stages tiles of the owner warp's segment (coalesced);
+        // the owner warp then walks it tile by tile: lane sums of 8 entries, a warp scan,
+        // and the first lane whose running sum passes the threshold resolves within its
+        // 8 entries
+        const int ow = cown[orank];
+        const int gwo = rank * (kDrawThreads / 32) + ow;
+        const int s0o = min(V, gwo * seg), s1o = min(V, s0o + seg);
+        const int ntiles = (s1o - s0o + 255) >> 8;
+        for (int t = warp; t < ntiles; t += kDrawThreads / 32) {
           float wv[8];
-          group_weights((s0 >> 3) + 32 * t + lane, mode, wv);
+          group_weights((s0o >> 3) + 32 * t + lane, mode, wv);
 #pragma unroll
           for (int e = 0; e < 8; ++e) wbuf[(t << 8) + (lane << 3) + e] = wv[e];
         }
-        __syncwarp();
-        float base = excl;
-        int pick = -1, lastpos = -1;
-        for (int t = 0; t < ntiles && pick < 0; ++t) {
-          const float* tw8 = wbuf + (t << 8) + (lane << 3);
-          float ls = 0.f;
-          int lp = -1;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            ls += tw8[e];
-            if (tw8[e] > 0.f) lp = (t << 8) + (lane << 3) + e;
-          }
-          float inc = ls;
-#pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, inc, off);
-            if (lane >= off) inc += y;
-          }
-          const unsigned hit = __ballot_sync(0xffffffffu, base + inc > target);
-          if (hit) {
-            const int hl = __ffs(hit) - 1;
-            int pk = -1;
-            if (lane == hl) {
-              float acc = base + inc - ls;
-              for (int e = 0; e < 8; ++e) {
-                acc += tw8[e];
-                if (acc > target) {
-                  pk = (t << 8) + (lane << 3) + e;
-                  break;
-                }
-              }
-              if (pk < 0) pk = lp;
+        __syncthreads();  // this CTA only: the owner CTA's warps all take this branch
+        if (warp == ow) {
+          float base = excl;
+          int pick = -1, lastpos = -1;
+          for (int t = 0; t < ntiles && pick < 0; ++t) {
+            const float* tw8 = wbuf + (t << 8) + (lane << 3);
+            float ls = 0.f;
+            int lp = -1;
+  #pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              ls += tw8[e];
+              if (tw8[e] > 0.f) lp = (t << 8) + (lane << 3) + e;
             }
-            pk = __shfl_sync(0xffffffffu, pk, hl);
-            // a run with no positive entry: the last positive one before it
-            const unsigned pos = __ballot_sync(0xffffffffu, lp >= 0) & (0xffffffffu >> (31 - hl));
-            if (pk < 0 && pos) pk = __shfl_sync(0xffffffffu, lp, 31 - __clz(pos));
-            if (pk < 0) pk = lastpos;
-            pick = pk;
-          } else {
-            const unsigned pos = __ballot_sync(0xffffffffu, lp >= 0);
-            if (pos) lastpos = __shfl_sync(0xffffffffu, lp, 31 - __clz(pos));
-            base += __shfl_sync(0xffffffffu, inc, 31);
+            float inc = ls;
+  #pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+              const float y = __shfl_up_sync(0xffffffffu, inc, off);
+              if (lane >= off) inc += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, base + inc > target);
+            if (hit) {
+              const int hl = __ffs(hit) - 1;
+              int pk = -1;
+              if (lane == hl) {
+                float acc = base + inc - ls;
+                for (int e = 0; e < 8; ++e) {
+                  acc += tw8[e];
+                  if (acc > target) {
+                    pk = (t << 8) + (lane << 3) + e;
+                    break;
+                  }
+                }
+                if (pk < 0) pk = lp;
+              }
+              pk = __shfl_sync(0xffffffffu, pk, hl);
+              // a run with no positive entry: the last positive one before it
+              const unsigned pos = __ballot_sync(0xffffffffu, lp >= 0) & (0xffffffffu >> (31 - hl));
+              if (pk < 0 && pos) pk = __shfl_sync(0xffffffffu, lp, 31 - __clz(pos));
+              if (pk < 0) pk = lastpos;
+              pick = pk;
+            } else {
+              const unsigned pos = __ballot_sync(0xffffffffu, lp >= 0);
+              if (pos) lastpos = __shfl_sync(0xffffffffu, lp, 31 - __clz(pos));
+              base += __shfl_sync(0xffffffffu, inc, 31);
+            }
           }
+          if (pick < 0) pick = lastpos;  // the threshold lies past every partial sum
+          if (lane == 0) P.next_token[i] = s0 + max(pick, 0);
         }
-        if (pick < 0) pick = lastpos;  // the threshold lies past every partial sum
-        if (lane == 0) P.next_token[i] = s0 + max(pick, 0);
       }
       break;
     }
