@@ -42,6 +42,7 @@ KERNEL_SOURCES = {
     "bwd_kernel": ("backward.cu", "common.cuh", "kernels.h"),
     "lse_rows_kernel": ("sampled.cu", "common.cuh", "kernels.h"),
     "sampled_draw_kernel": ("sampled.cu", "common.cuh", "kernels.h"),
+    "lmhead_gemm_kernel": ("lmhead.cu", "tc.cuh", "common.cuh", "kernels.h"),
 }
 
 
@@ -392,7 +393,8 @@ def run_ours(args):
                                  "frac": lm["tflops"] / tpeak, "rows_per_s": Nd / (lm["ms"] * 1e-3),
                                  "hidden": lm["hidden"], "vocab": lm["vocab"]}
         roofline_lmhead = {"bound": "tensor", "achieved": lm["tflops"], "peak": tpeak, "unit": "TFLOP/s",
-                           "frac": lm["tflops"] / tpeak, "traffic": None,
+                           "frac": lm["tflops"] / tpeak,
+                           "traffic": traffic.get("lmhead_gemm_kernel", {}).get("dram_bytes_per_launch"),
                            "kernel": "logit-free verify + loss forward (head GEMM dominant)",
                            "algorithmic_flops_per_launch": lm["flops"],
                            "peak_source": f"{tkind} (MEASURED_PEAKS.json bf16_tflops, burst)"}
