@@ -339,6 +339,9 @@ def run_ours(args):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
 
+    # concurrency 1 (one request of 16 draft rows): the step eager and replayed from a CUDA graph
+    small = run_small_batch_graph(dev, af, torch, np, make_workload, materialize)
+
     # the logit-free forward from hidden states at Qwen3-8B shapes (H = 4096, shared head),
     # the same packed layout as this workload
     lm = run_lmhead(args, w, dev, af, torch, np, stream)
@@ -409,7 +412,7 @@ def run_ours(args):
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; no datasets or weights)",
         "config": workload_config(w), "roofline": roofline, "roofline_fwd": roofline_fwd,
-        "roofline_lmhead": roofline_lmhead, "kernels": kernels,
+        "roofline_lmhead": roofline_lmhead, "kernels": kernels, "small_batch": small,
         "e2e": e2e, "gpu_launches": launches, "clocks": clk.summary(),
         "cpu_baseline": cpu_baseline(b) if world == 1 or rank == 0 else None,
         "impl": "ours",
@@ -427,6 +430,51 @@ def tensor_peak():
             return float(json.load(f)["bf16_tflops"]), "measured"
     except Exception:
         return 1900.0, "fallback"
+
+
+def run_small_batch_graph(dev, af, torch, np, make_workload, materialize):
+    """Concurrency 1 (`single`: 16 draft rows, 17 target rows): the single-call step eager,
+    and the same call captured once in a CUDA graph and replayed (launch-bound at this size)."""
+    b = materialize(make_workload("single"))
+    w = b.w
+    z = torch.from_numpy(b.draft.view(np.int16)).to(dev).view(torch.bfloat16)
+    t = torch.from_numpy(b.target.view(np.int16)).to(dev).view(torch.bfloat16)
+    tok, doff = torch.from_numpy(b.tokens).to(dev), torch.from_numpy(b.doff).to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream()
+    n = 200
+    with torch.cuda.stream(s):
+        out = af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_scale=1.0 / w.num_draft_rows,
+                                           status=st)
+        for _ in range(10):
+            af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_scale=1.0 / w.num_draft_rows,
+                                         out=out, status=st)
+        a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(n):
+            af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_scale=1.0 / w.num_draft_rows,
+                                         out=out, status=st)
+        bb.record(s)
+    s.synchronize()
+    eager_us = a.elapsed_time(bb) / n * 1e3
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_scale=1.0 / w.num_draft_rows,
+                                     out=out, status=st)
+    for _ in range(10):
+        graph.replay()
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(n):
+        graph.replay()
+    bb.record()
+    torch.cuda.synchronize()
+    graph_us = a.elapsed_time(bb) / n * 1e3
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())} (small batch)")
+    return {"workload": "single: 1 request, k = 16, V = 151936, bf16, fwd + bwd in one call (the on-chip fused kernel)",
+            "eager_us_per_step": eager_us, "graph_us_per_step": graph_us,
+            "rows_per_s_graph": w.num_draft_rows / (graph_us * 1e-6)}
 
 
 def run_lmhead(args, w, dev, af, torch, np, stream):
