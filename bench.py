@@ -339,6 +339,9 @@ def run_ours(args):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
 
+    # cold-HBM per-call times: an L2-sized flush (twice the L2) before every call
+    cold = run_cold(w, dev, af, torch, np, z, t, tok, doff, status, out, grad, stream)
+
     # concurrency 1 (one request of 16 draft rows): the step eager and replayed from a CUDA graph
     small = run_small_batch_graph(dev, af, torch, np, make_workload, materialize)
 
@@ -412,7 +415,7 @@ def run_ours(args):
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; no datasets or weights)",
         "config": workload_config(w), "roofline": roofline, "roofline_fwd": roofline_fwd,
-        "roofline_lmhead": roofline_lmhead, "kernels": kernels, "small_batch": small,
+        "roofline_lmhead": roofline_lmhead, "kernels": kernels, "small_batch": small, "cold": cold,
         "e2e": e2e, "gpu_launches": launches, "clocks": clk.summary(),
         "cpu_baseline": cpu_baseline(b) if world == 1 or rank == 0 else None,
         "impl": "ours",
@@ -430,6 +433,38 @@ def tensor_peak():
             return float(json.load(f)["bf16_tflops"]), "measured"
     except Exception:
         return 1900.0, "fallback"
+
+
+def run_cold(w, dev, af, torch, np, z, t, tok, doff, status, out, grad, stream, reps=21):
+    """Forward and backward calls each timed after writing twice the L2 size (cold HBM);
+    median and 10th / 90th percentiles over the reps."""
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (129 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    Nd = w.num_draft_rows
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * reps)]
+    for r in range(reps):
+        flush.fill_(r & 0xff)
+        a, b = ev[2 * r]
+        a.record(stream)
+        af.adaflash_opd_loss_fwd(z, t, tok, doff, w.clip_c, w.ce_weight, out=out, status=status)
+        b.record(stream)
+        flush.fill_((r + 1) & 0xff)
+        a, b = ev[2 * r + 1]
+        a.record(stream)
+        af.adaflash_opd_loss_bwd(z, t, doff, out["target_argmax"], out["row_stats"], w.clip_c, w.ce_weight,
+                                 grad_scale=1.0 / Nd, out=grad, status=status)
+        b.record(stream)
+    torch.cuda.synchronize()
+    fwd = sorted(ev[2 * r][0].elapsed_time(ev[2 * r][1]) * 1e3 for r in range(reps))
+    bwd = sorted(ev[2 * r + 1][0].elapsed_time(ev[2 * r + 1][1]) * 1e3 for r in range(reps))
+    del flush
+
+    def q(xs, f):
+        return xs[min(len(xs) - 1, int(round(f * (len(xs) - 1))))]
+
+    return {"flush_bytes": 2 * l2, "reps": reps,
+            "fwd_us": {"median": q(fwd, 0.5), "p10": q(fwd, 0.1), "p90": q(fwd, 0.9)},
+            "bwd_us": {"median": q(bwd, 0.5), "p10": q(bwd, 0.1), "p90": q(bwd, 0.9)}}
 
 
 def run_small_batch_graph(dev, af, torch, np, make_workload, materialize):

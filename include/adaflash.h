@@ -174,7 +174,7 @@ adaflash_status adaflash_opd_loss_fwd_bwd(
  * adaflash_verify_sampled -- temperature-sampled verification of packed draft blocks.
  *
  * The target verifies the drafted tokens in parallel (AdaFlash article, opening
- * section) at the sampling temperature, a tunable of the method (page "AdaFlash
+ * section) at the sampling temperature, a tunable of the method (page "Adaflash
  * Adaptive Speculative Decoding", section "Implementation Steps").  The rule is
  * speculative sampling, with p = softmax(z / T) of a draft row and q = softmax(t / T)
  * of its paired target row:

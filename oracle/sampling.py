@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE ONLY -- imported by ``tests/`` and never by the product path
 
 The AdaFlash article ("AdaFlash: Adaptive Speculative Decoding with Online
 Self-Improvement for High-Concurrency LLM Inference", opening section) describes
-the target verifying drafted tokens in parallel; the skill card "AdaFlash
+the target verifying drafted tokens in parallel; the skill card "Adaflash
 Adaptive Speculative Decoding", section "Implementation Steps", lists the
 temperature as a tunable.  With a temperature the verification is the standard
 speculative-sampling rule, taken here as the plainest reading:

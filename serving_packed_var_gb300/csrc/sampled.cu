@@ -3,7 +3,7 @@
 // The target verifies the drafted tokens in parallel (AdaFlash article, "AdaFlash:
 // Adaptive Speculative Decoding with Online Self-Improvement for High-Concurrency
 // LLM Inference", opening section); the temperature is a tunable of the method
-// (skill card "AdaFlash Adaptive Speculative Decoding", "Implementation Steps").
+// (skill card "Adaflash Adaptive Speculative Decoding", "Implementation Steps").
 // With p = softmax(z/T) and q = softmax(t/T) the rule is speculative sampling:
 //
 //   token j is accepted when u_j p(x_j) < q(x_j);
