@@ -50,24 +50,33 @@ namespace adaflash {
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
+#ifndef ADAFLASH_ROWPASS_CONSUMER_WARPS
+#define ADAFLASH_ROWPASS_CONSUMER_WARPS 8
+#endif
+constexpr int kConsumerWarps = ADAFLASH_ROWPASS_CONSUMER_WARPS;
+static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "a power-of-two number of consumer warps");
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
-// Ring depth and resident CTAs per SM (compile-time tuning; the defaults are the
-// measured best on GB300 for bf16 logits).
+// Ring depth, stage size and resident CTAs per SM (compile-time tuning; the
+// defaults are the measured best on GB300 for bf16 logits: two CTAs per SM, each
+// with a 96 KB ring of three 8192-entry stages of z and t).
 #ifndef ADAFLASH_ROWPASS_STAGES
 #define ADAFLASH_ROWPASS_STAGES 3
 #endif
 #ifndef ADAFLASH_ROWPASS_MINBLOCKS
-#define ADAFLASH_ROWPASS_MINBLOCKS 3
+#define ADAFLASH_ROWPASS_MINBLOCKS 2
 #endif
 constexpr int kStages = ADAFLASH_ROWPASS_STAGES;
 #ifndef ADAFLASH_ROWPASS_CHUNK
-#define ADAFLASH_ROWPASS_CHUNK 4096
+#define ADAFLASH_ROWPASS_CHUNK 8192
 #endif
-constexpr int kChunk = ADAFLASH_ROWPASS_CHUNK;  // entries of each tensor per stage
-constexpr int kGroupsPerThread = kChunk / 8 / 256;  // 8-entry groups per consumer thread per chunk
-static_assert(kGroupsPerThread >= 1 && kChunk % 2048 == 0, "a chunk gives every consumer thread whole groups");
+// Entries of each tensor per stage: ADAFLASH_ROWPASS_CHUNK for two 16-bit inputs,
+// half of it when either input is float32 (the same ring bytes).
+template <class DZ, class DT>
+__host__ __device__ constexpr int chunk_of() {
+  return DZ::kBytes + DT::kBytes <= 4 ? ADAFLASH_ROWPASS_CHUNK : ADAFLASH_ROWPASS_CHUNK / 2;
+}
+static_assert((ADAFLASH_ROWPASS_CHUNK / 2) % (8 * kConsumers) == 0, "a chunk gives every consumer thread whole groups");
 
 }  // namespace
 
@@ -99,6 +108,8 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
   const int ncl = static_cast<int>(gridDim.x) / C;
   const int num_units = P.unit_end;
 
+  constexpr int kChunk = chunk_of<DZ, DT>();
+  constexpr int kGroupsPerThread = kChunk / 8 / kConsumers;  // 8-entry groups per consumer thread per chunk
   constexpr int kStageZ = kChunk * DZ::kBytes;
   constexpr int kStageT = kChunk * DT::kBytes;
   // 128-byte aligned base for the bulk-copy ring (the launch adds 128 bytes of slack).
@@ -201,10 +212,11 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
                 float z[8], t[8], vmz, vmt;
                 load8_smem<DZ>(stage, g, z, vmz);
                 load8_smem<DT>(stage + kStageZ, g, t, vmt);
-                acc_pair(acc, z, t, vmz, vmt, gbase + g);
+                acc_pair_nc(acc, z, t, vmz, vmt, gbase + g);
                 cm = fmaxf(cm, vmz);
               }
             }
+            acc.cmax = fmaxf(acc.cmax, cm);
             codes[(e0 / kChunk) * kConsumers + tid] = code_up(cm);
           } else {
 #pragma unroll
@@ -442,11 +454,11 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
 
 int rowpass_cluster_size(int vocab, int units, int num_sms) {
   // At most ADAFLASH_ROWPASS_SLICE_TARGET entries per CTA, and enough CTAs in
-  // flight to fill the GPU (3 per SM) when there are few rows; at most 8 (the
+  // flight to fill the GPU (the resident CTAs per SM) when there are few rows; at most 8 (the
   // portable cluster size).
   int c = (vocab + ADAFLASH_ROWPASS_SLICE_TARGET - 1) / ADAFLASH_ROWPASS_SLICE_TARGET;
   if (c < 1) c = 1;
-  while (c < kMaxCluster && static_cast<long long>(units) * c < 3LL * num_sms) ++c;
+  while (c < kMaxCluster && static_cast<long long>(units) * c < static_cast<long long>(ADAFLASH_ROWPASS_MINBLOCKS) * num_sms) ++c;
   return c > kMaxCluster ? kMaxCluster : c;
 }
 
@@ -481,6 +493,7 @@ static int sm_count() {
 
 template <class DZ, class DT, bool kFast>
 static size_t rowpass_smem(int slice) {
+  constexpr int kChunk = chunk_of<DZ, DT>();
   const size_t ring = static_cast<size_t>(kStages) * kChunk * (DZ::kBytes + DT::kBytes);
   // screening codes: per consumer thread one slot per ring chunk (+1 for a ragged
   // tail group) on the bulk-copy path, one per group on the direct-load path

@@ -139,23 +139,19 @@ __device__ __forceinline__ float code_value(uint16_t c) { return __uint_as_float
 // 2^{x log2e + n} is 0 and z - t is 0.
 constexpr float kVoid = -1.0e30f;
 
-// Paired group of 8 entries, row-global group index grp (unused entries of z and t
-// hold kVoid).  vmz = max z, vmt = max t over the valid entries.
-__device__ __forceinline__ void acc_pair(Acc& a, const float z[8], const float t[8], float vmz, float vmt,
-                                         int grp) {
-  if (vmz > a.zlim) rescale_z(a, vmz);
-  if (vmt > a.tlim) rescale_t(a, vmt);
+// Sums of one paired group of 8 entries at the current offsets (no rescale check,
+// no maxima of z): the caller has moved the offsets for this group's maxima.
+__device__ __forceinline__ void acc_pair_sums(Acc& a, const float z[8], const float t[8], float vmt, int grp) {
   const bool nb = vmt > a.mt;
   a.mt = fmaxf(a.mt, vmt);
   a.bgrp = nb ? grp : a.bgrp;
-  a.cmax = fmaxf(a.cmax, vmz);
   {
     // Two entries per instruction on the FMA pipe (f32x2): even/odd entries are the
     // two lanes of each packed register, matching the two accumulators.
     const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
     const uint64_t nz2 = f2_pack(a.nzf, a.nzf), nt2 = f2_pack(a.ntf, a.ntf);
     uint64_t SZ = f2_pack(a.sz0, a.sz1), ST = f2_pack(a.st0, a.st1), SD = f2_pack(a.szd0, a.szd1);
-    float dm0 = a.dmax, dm1 = kNegInf;
+    float dm = a.dmax;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint64_t Z = f2_pack(z[2 * q], z[2 * q + 1]);
@@ -170,14 +166,30 @@ __device__ __forceinline__ void acc_pair(Acc& a, const float z[8], const float t
       SD = f2_fma(EZ, D, SD);
       float d0, d1;
       f2_unpack(D, d0, d1);
-      dm0 = fmaxf(dm0, d0);
-      dm1 = fmaxf(dm1, d1);
+      dm = fmax3f(dm, d0, d1);
     }
     f2_unpack(SZ, a.sz0, a.sz1);
     f2_unpack(ST, a.st0, a.st1);
     f2_unpack(SD, a.szd0, a.szd1);
-    a.dmax = fmaxf(dm0, dm1);
+    a.dmax = dm;
   }
+}
+
+// Paired group of 8 entries, row-global group index grp (unused entries of z and t
+// hold kVoid).  vmz = max z, vmt = max t over the valid entries.  The caller keeps
+// a.cmax (the largest group maximum of z) up to date.
+__device__ __forceinline__ void acc_pair_nc(Acc& a, const float z[8], const float t[8], float vmz, float vmt,
+                                            int grp) {
+  if (vmz > a.zlim) rescale_z(a, vmz);
+  if (vmt > a.tlim) rescale_t(a, vmt);
+  acc_pair_sums(a, z, t, vmt, grp);
+}
+
+// The same, updating a.cmax.
+__device__ __forceinline__ void acc_pair(Acc& a, const float z[8], const float t[8], float vmz, float vmt,
+                                         int grp) {
+  acc_pair_nc(a, z, t, vmz, vmt, grp);
+  a.cmax = fmaxf(a.cmax, vmz);
 }
 
 // Target-only group: argmax only.
@@ -202,15 +214,18 @@ __device__ int resolve_argmax(const uint8_t* trow, int grp, float mt, int V) {
 template <class DT>
 __device__ __forceinline__ void load8_smem(const uint8_t* base, int g, float x[8], float& vmax);
 
+__device__ __forceinline__ float max8(const float x[8]) {
+  return fmax3f(fmax3f(x[0], x[1], x[2]), fmax3f(x[3], x[4], x[5]), fmaxf(x[6], x[7]));
+}
+
 template <>
 __device__ __forceinline__ void load8_smem<BF16>(const uint8_t* base, int g, float x[8], float& vmax) {
   const uint4 q = *reinterpret_cast<const uint4*>(base + 16 * g);
-  const uint32_t m = bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w));
-  vmax = fmaxf(bf16_lo(m), bf16_hi(m));
   x[0] = bf16_lo(q.x); x[1] = bf16_hi(q.x);
   x[2] = bf16_lo(q.y); x[3] = bf16_hi(q.y);
   x[4] = bf16_lo(q.z); x[5] = bf16_hi(q.z);
   x[6] = bf16_lo(q.w); x[7] = bf16_hi(q.w);
+  vmax = max8(x);
 }
 
 template <>
@@ -219,7 +234,7 @@ __device__ __forceinline__ void load8_smem<F32>(const uint8_t* base, int g, floa
   const float4 b = *reinterpret_cast<const float4*>(base + 32 * g + 16);
   x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
   x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  vmax = fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
+  vmax = max8(x);
 }
 
 // Up to 8 entries straight from global memory (any alignment); unused entries get kVoid.
