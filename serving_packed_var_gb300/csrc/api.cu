@@ -16,6 +16,13 @@ using namespace adaflash;
 
 namespace {
 
+// adaflash_opd_loss_fwd_bwd on more than a wave of row units: 1 = the single-pass
+// row pass with the gradient, 0 = the forward row pass, then the backward.
+#ifndef ADAFLASH_FWDBWD_STREAM
+#define ADAFLASH_FWDBWD_STREAM 1
+#endif
+constexpr bool kFwdBwdStream = ADAFLASH_FWDBWD_STREAM != 0;
+
 bool valid_dtype(adaflash_dtype t) { return t == ADAFLASH_FP32 || t == ADAFLASH_BF16; }
 int dtype_bytes(adaflash_dtype t) { return t == ADAFLASH_FP32 ? 4 : 2; }
 
@@ -315,11 +322,18 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
   const bool fast = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
                     rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)) && rows_16b(grad_draft, ld_g, 4);
   const bool fused = fast && num_draft_rows + num_requests <= fused_max_units(vocab, d_dtype, t_dtype, num_sms());
+  const bool stream_grad = fast && !fused && kFwdBwdStream;
   if (fused) {
     ADAFLASH_CUDA(launch_fused(p, d_dtype, t_dtype, num_sms(), s));
+  } else if (stream_grad) {
+    // more than a wave of row units: one streaming pass per row slice that reads the
+    // logits from HBM once and writes dz from a second pass served by L2
+    const int row_bytes = vocab * (dtype_bytes(d_dtype) + dtype_bytes(t_dtype));
+    p.cluster = rowpass_grad_cluster_size(vocab, p.N_d + p.R, row_bytes, num_sms());
+    p.slice = rowpass_slice(vocab, p.cluster);
+    ADAFLASH_CUDA(launch_rowpass_grad(p, d_dtype, t_dtype, s));
   } else {
-    // rows off the 16-byte grid, a vocabulary too large to hold on chip, or a batch of
-    // more than a wave of row units: the streaming forward, then the streaming backward
+    // rows off the 16-byte grid: the streaming forward, then the streaming backward
     p.cluster = rowpass_cluster_size(vocab, p.N_d + p.R, num_sms());
     p.slice = rowpass_slice(vocab, p.cluster);
     ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype,
@@ -345,7 +359,7 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
   f.status = d_status;
   ADAFLASH_CUDA(launch_finalize(f, s));
 
-  if (!fused) {
+  if (!fused && !stream_grad) {
     BwdParams b = {};
     b.z = draft_logits;
     b.t = target_logits;

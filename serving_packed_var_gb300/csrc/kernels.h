@@ -28,7 +28,7 @@ struct RowPassParams {
   float* ce_row;
   float* row_stats;
   uint32_t* status;
-  // fused forward + backward only (K4)
+  // fused forward + backward only (K4, and the row pass with the gradient)
   float ce_weight;
   const float* grad_row;  // NULL: grad_scale for every row
   float grad_scale;
@@ -130,6 +130,10 @@ void count_launch();
 
 // dtype codes match adaflash_dtype (0 = fp32, 1 = bf16)
 cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
+// The row pass with the gradient (single-pass forward + backward; rows on the
+// 16-byte grid).  Cluster size: rowpass_grad_cluster_size (row_bytes = V (b_z + b_t)).
+cudaError_t launch_rowpass_grad(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s);
+int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int num_sms);
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
 // Fused forward + backward (K4).  fused_max_units is the largest batch (draft rows +

@@ -80,7 +80,35 @@ static_assert((ADAFLASH_ROWPASS_CHUNK / 2) % (8 * kConsumers) == 0, "a chunk giv
 
 }  // namespace
 
-template <class DZ, class DT, bool kFast>
+// Per-row coefficients of the gradient (the backward's per-entry sequence).
+struct RowGrad {
+  TermConsts tc;
+  float c;
+  float k_m;     // 1 + beta - S   (inner factor where the term is kept: r + k_m)
+  float k_clip;  // beta - S       (inner factor where the term is clipped)
+  float g;       // upstream weight of the row
+  float bg;      // beta * g, taken off at the target argmax
+  float lse_z;
+  float mt;      // the max of t
+  int ga;        // slice-local group holding the first max of t, -1 when not in this slice
+  int stop;      // a wait gave up: every consumer thread leaves together
+};
+
+__device__ __forceinline__ float grad_of(float z, float t, const RowGrad& k) {
+  float p, r, term;
+  entry_term(z, t, k.tc, p, r, term);
+  const float inner = (term <= k.c) ? __fadd_rn(r, k.k_m) : k.k_clip;
+  return __fmul_rn(__fmul_rn(p, inner), k.g);
+}
+
+// kGrad: the single-pass forward + backward for batches of many rows.  After a
+// pair unit's row constants and clip corrections are known, the producer's second
+// pass over the same slice (queued right behind the first, so it is served from L2:
+// the first pass asks L2 to keep the lines, the second to drop them) feeds the
+// gradient, dz_v = g (p_v (m_v (r_v + 1) - S) + beta (p_v - [v == a])), written once
+// with streaming stores.  Every CTA of the cluster gets the corrections (every CTA
+// needs S).
+template <class DZ, class DT, bool kFast, bool kGrad>
 __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_kernel(const RowPassParams P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages];
@@ -93,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
   __shared__ float warp_corr[kConsumerWarps][2];
   __shared__ int warp_nclip[kConsumerWarps];
   __shared__ RowConsts rc;
+  __shared__ RowGrad s_grad;
   __shared__ int s_abort;
   __shared__ int s_unit_err;
 
@@ -141,6 +170,11 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
     // ---------------- producer warp: runs ahead across units ----------------
     if (kFast && lane == 0) {
       uint32_t cc = 0;
+      uint64_t keep = 0, drop = 0;
+      if (kGrad) {
+        keep = l2_policy_evict_last();
+        drop = l2_policy_evict_first();
+      }
       for (int u = P.unit_begin + cid; u < num_units && !*abort_flag; u += ncl) {
         const Unit U = map_unit(P, u);
         const int v_begin = static_cast<int>(rank) * P.slice;
@@ -150,20 +184,31 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
             U.pair ? static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(U.d) * P.ld_z * DZ::kBytes : nullptr;
         const uint8_t* trow =
             static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(max(U.s, 0)) * P.ld_t * DT::kBytes;
-        for (int e0 = 0; e0 < body; e0 += kChunk, ++cc) {
-          const int st = static_cast<int>(cc % kStages);
-          if (cc >= static_cast<uint32_t>(kStages) &&
-              !mbar_wait_bounded(&empty_bar[st], ((cc / kStages) & 1) ^ 1)) {
-            *abort_flag = 1;
-            break;
+        const int passes = (kGrad && U.pair && !U.bad) ? 2 : 1;
+        for (int pass = 0; pass < passes && !*abort_flag; ++pass) {
+          for (int e0 = 0; e0 < body; e0 += kChunk, ++cc) {
+            const int st = static_cast<int>(cc % kStages);
+            if (cc >= static_cast<uint32_t>(kStages) &&
+                !mbar_wait_bounded(&empty_bar[st], ((cc / kStages) & 1) ^ 1)) {
+              *abort_flag = 1;
+              break;
+            }
+            const int n = min(kChunk, body - e0);
+            const uint32_t bz = U.pair ? static_cast<uint32_t>(n * DZ::kBytes) : 0u;
+            const uint32_t bt = static_cast<uint32_t>(n * DT::kBytes);
+            mbar_arrive_expect_tx(&full_bar[st], bz + bt);
+            uint8_t* stage = ring + st * (kStageZ + kStageT);
+            const uint8_t* zsrc = zrow + static_cast<int64_t>(v_begin + e0) * DZ::kBytes;
+            const uint8_t* tsrc = trow + static_cast<int64_t>(v_begin + e0) * DT::kBytes;
+            if (kGrad && U.pair) {
+              const uint64_t pol = pass == 0 ? keep : drop;
+              bulk_copy_g2s_hint(stage, zsrc, bz, &full_bar[st], pol);
+              bulk_copy_g2s_hint(stage + kStageZ, tsrc, bt, &full_bar[st], pol);
+            } else {
+              if (U.pair) bulk_copy_g2s(stage, zsrc, bz, &full_bar[st]);
+              bulk_copy_g2s(stage + kStageZ, tsrc, bt, &full_bar[st]);
+            }
           }
-          const int n = min(kChunk, body - e0);
-          const uint32_t bz = U.pair ? static_cast<uint32_t>(n * DZ::kBytes) : 0u;
-          const uint32_t bt = static_cast<uint32_t>(n * DT::kBytes);
-          mbar_arrive_expect_tx(&full_bar[st], bz + bt);
-          uint8_t* stage = ring + st * (kStageZ + kStageT);
-          if (U.pair) bulk_copy_g2s(stage, zrow + static_cast<int64_t>(v_begin + e0) * DZ::kBytes, bz, &full_bar[st]);
-          bulk_copy_g2s(stage + kStageZ, trow + static_cast<int64_t>(v_begin + e0) * DT::kBytes, bt, &full_bar[st]);
         }
       }
       // After an abort, let copies still in flight land before the CTA can exit.
@@ -280,8 +325,13 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
         }
         SlicePartial all;
         combine_partials(slots[buf], C, all);
-        // The lowest index of the maximum lies in the first group holding it.
-        rc.argmax = (rank == 0 && !U.bad) ? resolve_argmax<DT>(trow, all.bgrp, all.mt, P.V) : -1;
+        // The lowest index of the maximum lies in the first group holding it.  With the
+        // gradient, a pair row's index is found in the second pass by the thread that
+        // holds that group (no re-read here).
+        rc.bgrp = all.bgrp;
+        rc.mt = all.mt;
+        rc.argmax = (rank == 0 && !U.bad && !(kGrad && U.pair)) ? resolve_argmax<DT>(trow, all.bgrp, all.mt, P.V)
+                                                                 : -1;
         rc.err = all.err | werr;
         rc.stop = *abort_flag;
         if (U.pair && !U.bad) {
@@ -326,6 +376,15 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
       auto finish_row = [&](float corr_all, float sclip_all, int nclip_all, int err_all) {
         if (U.bad) {
           flag_status(P.status, ADAFLASH_ERR_BAD_OFFSETS);
+        } else if (kGrad) {
+          // the argmax and the cross-entropy come from the second pass
+          const int64_t d = U.d;
+          P.kl_row[d] = rc.kl_unclip - corr_all;
+          P.row_stats[4 * d + 0] = rc.lse_z;
+          P.row_stats[4 * d + 1] = rc.lse_t;
+          P.row_stats[4 * d + 2] = (rc.kl_unclip + 1.f) - sclip_all;
+          P.row_stats[4 * d + 3] = static_cast<float>(nclip_all);
+          if (err_all || rc.bgrp < 0 || rc.bgrp >= (P.V + 7) / 8) flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
         } else if (rc.argmax < 0 || rc.argmax >= P.V) {
           // only after an aborted unit (no group was reduced): nothing valid to write
           flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
@@ -342,11 +401,33 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
           if (err_all) flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
         }
       };
+      // Gradient coefficients of the row from the summed corrections (tid 0), the
+      // same float32 expressions as the stored row statistics the backward reads.
+      auto set_grad = [&](float sclip_all) {
+        const float S = (rc.kl_unclip + 1.f) - sclip_all;
+        RowGrad k;
+        k.tc = make_term_consts(rc.lse_z, rc.lse_t);
+        k.c = P.clip_c;
+        k.k_clip = __fsub_rn(P.ce_weight, S);
+        k.k_m = __fadd_rn(1.0f, k.k_clip);
+        k.g = P.grad_row ? __ldg(P.grad_row + U.d) : P.grad_scale;
+        k.bg = __fmul_rn(P.ce_weight, k.g);
+        k.lse_z = rc.lse_z;
+        k.mt = rc.mt;
+        const int ga = rc.bgrp - (v_begin >> 3);
+        k.ga = (ga >= 0 && ga < ngroups) ? ga : -1;
+        k.stop = *abort_flag;
+        s_grad = k;
+      };
       if (!rc.any_scan) {
         if (rank == 0 && tid == 0) finish_row(0.f, 0.f, 0, rc.err);
-        if (stop) break;
-        continue;
-      }
+        if constexpr (!kGrad) {
+          if (stop) break;
+          continue;
+        } else {
+          if (tid == 0) set_grad(0.f);
+        }
+      } else {
 
       // ---- exact evaluation of the screened groups ----
       float corr = 0.f, sclip = 0.f;
@@ -376,11 +457,22 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
               }
               const int v0 = v_begin + (g << 3);
               const int n = min(8, v_end - v0);
-              for (int j = 0; j < n; ++j) {
-                const float zv = DZ::load(zrow, v0 + j);
-                const float tv = DT::load(trow, v0 + j);
+              float zs[8], ts[8];
+              if (kFast && n == 8) {
+                load8_global_vec<DZ>(zrow, v0, zs);
+                load8_global_vec<DT>(trow, v0, ts);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  zs[j] = j < n ? DZ::load(zrow, v0 + j) : 0.f;
+                  ts[j] = j < n ? DT::load(trow, v0 + j) : 0.f;
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                if (j >= n) break;
                 float p, r, term;
-                entry_term(zv, tv, tc, p, r, term);  // the backward's evaluation, bit for bit
+                entry_term(zs[j], ts[j], tc, p, r, term);  // the backward's evaluation, bit for bit
                 if (term > c) {
                   corr += term - c;
                   sclip = fmaf(p, r + 1.f, sclip);
@@ -412,9 +504,11 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
           mine.sclip += warp_corr[w][1];
           mine.nclip += warp_nclip[w];
         }
-        *map_to_rank(&cslots[cbuf][rank], 0u) = mine;
-        mbar_arrive_remote(&corr_bar[cbuf], 0u);
-        if (rank == 0) {
+        // To rank 0 only; with the gradient, to every CTA (each needs S).
+        const int nto = kGrad ? C : 1;
+        for (int r = 0; r < nto; ++r) *map_to_rank(&cslots[cbuf][rank], static_cast<uint32_t>(r)) = mine;
+        for (int r = 0; r < nto; ++r) mbar_arrive_remote(&corr_bar[cbuf], static_cast<uint32_t>(r));
+        if (kGrad || rank == 0) {
           const bool ok = mbar_wait_cluster_bounded(&corr_bar[cbuf], (pit >> 1) & 1);
           if (!ok) *abort_flag = 1;
           float corr_all = 0.f, sclip_all = 0.f;
@@ -425,11 +519,91 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
             nclip_all += cslots[cbuf][r].nclip;
             err_all |= cslots[cbuf][r].err;
           }
-          finish_row(corr_all, sclip_all, nclip_all, err_all);
+          if (rank == 0) finish_row(corr_all, sclip_all, nclip_all, err_all);
+          if (kGrad) set_grad(sclip_all);
         }
       }
       ++pit;
-      if (stop) break;
+      }  // any_scan
+      if constexpr (kGrad) {
+        named_bar_sync(kConsumers);  // s_grad is set
+        if (stop || s_grad.stop) break;
+        if (!U.bad) {
+          // ---- second pass over the slice (from L2): dz, written once ----
+          const RowGrad k = s_grad;
+          float* grow = P.grad + static_cast<int64_t>(U.d) * P.ld_g + v_begin;
+          for (int e0 = 0; e0 < body; e0 += kChunk, ++cc) {
+            const int st = static_cast<int>(cc % kStages);
+            if (!mbar_wait_bounded(&full_bar[st], (cc / kStages) & 1)) {
+              atomicOr(&s_unit_err, 1);
+              *abort_flag = 1;
+              break;
+            }
+            const int gcount = min(kChunk, body - e0) >> 3;
+            const uint8_t* stage = ring + st * (kStageZ + kStageT);
+#pragma unroll
+            for (int kk = 0; kk < kGroupsPerThread; ++kk) {
+              const int g = tid + kk * kConsumers;
+              if (g < gcount) {
+                float z[8], t[8], out[8], vm;
+                load8_smem<DZ>(stage, g, z, vm);
+                load8_smem<DT>(stage + kStageZ, g, t, vm);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) out[e] = grad_of(z[e], t[e], k);
+                float4* dst = reinterpret_cast<float4*>(grow + e0 + (g << 3));
+                __stcs(dst, make_float4(out[0], out[1], out[2], out[3]));
+                __stcs(dst + 1, make_float4(out[4], out[5], out[6], out[7]));
+              }
+            }
+            // The group holding the first max of t: the thread that just wrote it finds
+            // the index, rewrites that entry with the hard-label term (program order makes
+            // it the final value) and writes the argmax and the cross-entropy.
+            const int lc = k.ga - (e0 >> 3);
+            if (lc >= 0 && lc < gcount && tid == (lc & (kConsumers - 1))) {
+              float zz[8], tt[8], vm;
+              load8_smem<DZ>(stage, lc, zz, vm);
+              load8_smem<DT>(stage + kStageZ, lc, tt, vm);
+              int j = -1;
+              float zj = 0.f, tj = 0.f;
+#pragma unroll
+              for (int e = 7; e >= 0; --e)
+                if (tt[e] == k.mt) {
+                  j = e;
+                  zj = zz[e];
+                  tj = tt[e];
+                }
+              if (j >= 0) {
+                const int la = e0 + (lc << 3) + j;
+                grow[la] = __fsub_rn(grad_of(zj, tj, k), k.bg);
+                P.target_argmax[U.s] = v_begin + la;
+                P.ce_row[U.d] = k.lse_z - zj;
+              } else {
+                flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[st]);
+          }
+          // the ragged end of the slice (fewer than 8 entries) straight from global memory;
+          // each entry is written by one thread, the argmax by the thread holding it
+          for (int v = body + tid; v < len; v += kConsumers) {
+            const float zv = DZ::load(zrow, v_begin + v), tv = DT::load(trow, v_begin + v);
+            float o = grad_of(zv, tv, k);
+            if (k.ga == (body >> 3) && tv == k.mt) {
+              bool first = true;
+              for (int u = body; u < v; ++u) first = first && !(DT::load(trow, v_begin + u) == k.mt);
+              if (first) {
+                o = __fsub_rn(o, k.bg);
+                P.target_argmax[U.s] = v_begin + v;
+                P.ce_row[U.d] = k.lse_z - zv;
+              }
+            }
+            grow[v] = o;
+          }
+        }
+      } else {
+        if (stop) break;
+      }
     }
     if (*abort_flag && tid == 0) flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
   }
@@ -491,7 +665,7 @@ static int sm_count() {
   return n;
 }
 
-template <class DZ, class DT, bool kFast>
+template <class DZ, class DT, bool kFast, bool kGrad>
 static size_t rowpass_smem(int slice) {
   constexpr int kChunk = chunk_of<DZ, DT>();
   const size_t ring = static_cast<size_t>(kStages) * kChunk * (DZ::kBytes + DT::kBytes);
@@ -503,9 +677,9 @@ static size_t rowpass_smem(int slice) {
 }
 
 // Co-resident clusters of this kernel at this cluster size (cached).
-template <class DZ, class DT, bool kFast>
+template <class DZ, class DT, bool kFast, bool kGrad>
 static int active_clusters(int cluster, size_t smem) {
-  auto kern = rowpass_kernel<DZ, DT, kFast>;
+  auto kern = rowpass_kernel<DZ, DT, kFast, kGrad>;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return 1;
   // The query must see the shared-memory size the launch will use.
@@ -539,15 +713,15 @@ static int active_clusters(int cluster, size_t smem) {
 }
 
 // One launch over units [p.unit_begin, p.unit_end), persistent clusters.
-template <class DZ, class DT, bool kFast>
+template <class DZ, class DT, bool kFast, bool kGrad>
 static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaStream_t stream) {
-  const size_t smem = rowpass_smem<DZ, DT, kFast>(p.slice);
-  auto kern = rowpass_kernel<DZ, DT, kFast>;
+  const size_t smem = rowpass_smem<DZ, DT, kFast, kGrad>(p.slice);
+  auto kern = rowpass_kernel<DZ, DT, kFast, kGrad>;
   const int units = p.unit_end - p.unit_begin;
   if (units <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int clusters = active_clusters<DZ, DT, kFast>(p.cluster, smem);
+  const int clusters = active_clusters<DZ, DT, kFast, kGrad>(p.cluster, smem);
   cudaLaunchConfig_t cfg = {};
   const int grid_clusters = units < clusters ? units : clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters) * static_cast<unsigned>(p.cluster), 1, 1);
@@ -573,7 +747,7 @@ static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaS
 // over more CTAs instead of leaving a few CTAs to finish whole rows alone.  The
 // second launch starts as CTAs of the first retire (programmatic launch) and
 // completes only after the first.
-template <class DZ, class DT, bool kFast>
+template <class DZ, class DT, bool kFast, bool kGrad = false>
 static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   const int units = (p0.mode == kModeVerify) ? p0.N_t : (p0.N_d + p0.R);
   if (units <= 0) return cudaSuccess;
@@ -581,13 +755,13 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   p.unit_begin = 0;
   p.unit_end = units;
   p.wait_prior = 0;
-  const int clusters = active_clusters<DZ, DT, kFast>(p.cluster, rowpass_smem<DZ, DT, kFast>(p.slice));
+  const int clusters = active_clusters<DZ, DT, kFast, kGrad>(p.cluster, rowpass_smem<DZ, DT, kFast, kGrad>(p.slice));
   const int split = (units / clusters) * clusters;
   if (!ADAFLASH_ROWPASS_TAIL || units <= clusters || split == units || p.cluster >= kMaxCluster)
-    return launch_range<DZ, DT, kFast>(p, false, stream);
+    return launch_range<DZ, DT, kFast, kGrad>(p, false, stream);
   RowPassParams tail = p;
   p.unit_end = split;
-  cudaError_t e = launch_range<DZ, DT, kFast>(p, false, stream);
+  cudaError_t e = launch_range<DZ, DT, kFast, kGrad>(p, false, stream);
   if (e != cudaSuccess) return e;
   tail.unit_begin = split;
   tail.unit_end = units;
@@ -595,7 +769,30 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   tail.cluster = rowpass_cluster_size(p.V, units - split, sm_count());
   if (tail.cluster < p.cluster) tail.cluster = p.cluster;
   tail.slice = rowpass_slice(p.V, tail.cluster);
-  return launch_range<DZ, DT, kFast>(tail, true, stream);
+  return launch_range<DZ, DT, kFast, kGrad>(tail, true, stream);
+}
+
+#ifndef ADAFLASH_FWDBWD_L2_BUDGET
+#define ADAFLASH_FWDBWD_L2_BUDGET (96ll << 20)  // bytes of rows in flight in the single-pass forward + backward
+#endif
+
+int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int num_sms) {
+  // The row pass's size, raised until the rows in flight at once (resident CTAs /
+  // C rows of row_bytes) fit the L2 budget, so that the second pass over each slice
+  // is served from L2.
+  int c = rowpass_cluster_size(vocab, units, num_sms);
+  while (c < kMaxCluster && static_cast<long long>(ADAFLASH_ROWPASS_MINBLOCKS) * num_sms / c * row_bytes >
+                                ADAFLASH_FWDBWD_L2_BUDGET)
+    ++c;
+  return c;
+}
+
+cudaError_t launch_rowpass_grad(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s) {
+  const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
+  if (zb && tb) return launch_one<BF16, BF16, true, true>(p, s);
+  if (!zb && tb) return launch_one<F32, BF16, true, true>(p, s);
+  if (zb && !tb) return launch_one<BF16, F32, true, true>(p, s);
+  return launch_one<F32, F32, true, true>(p, s);
 }
 
 cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s) {

@@ -45,6 +45,8 @@ struct RowConsts {
   float lse_z, lse_t, dlse, kl_unclip;
   float theta;
   int argmax;
+  int bgrp;  // first (row-global) group holding the max of t
+  float mt;  // the max of t
   int err;
   int stop;  // every consumer thread leaves the unit loop together when set
   int scan;      // some thread of this CTA saw a group maximum of z above the threshold
@@ -235,6 +237,26 @@ __device__ __forceinline__ void load8_smem<F32>(const uint8_t* base, int g, floa
   x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
   x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
   vmax = max8(x);
+}
+
+// 8 entries from global memory with vector loads (v0 a multiple of 8, row on the
+// 16-byte grid).
+template <class DT>
+__device__ __forceinline__ void load8_global_vec(const uint8_t* row, int64_t v0, float x[8]);
+template <>
+__device__ __forceinline__ void load8_global_vec<BF16>(const uint8_t* row, int64_t v0, float x[8]) {
+  const uint4 q = __ldg(reinterpret_cast<const uint4*>(row + v0 * 2));
+  x[0] = bf16_lo(q.x); x[1] = bf16_hi(q.x);
+  x[2] = bf16_lo(q.y); x[3] = bf16_hi(q.y);
+  x[4] = bf16_lo(q.z); x[5] = bf16_hi(q.z);
+  x[6] = bf16_lo(q.w); x[7] = bf16_hi(q.w);
+}
+template <>
+__device__ __forceinline__ void load8_global_vec<F32>(const uint8_t* row, int64_t v0, float x[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(row + v0 * 4));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(row + v0 * 4 + 16));
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
 // Up to 8 entries straight from global memory (any alignment); unused entries get kVoid.

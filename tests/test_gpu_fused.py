@@ -141,6 +141,39 @@ def test_edge_shapes(case):
     _close_to_separate(b, oracle_grad_rows=gsel)
 
 
+# More than one wave of row units: the single-pass row pass with the gradient (each
+# slice read from HBM once; the second pass over it, for dz, is served by L2).
+STREAM = [
+    dict(vocab=151936, k=[16] * 8),
+    dict(vocab=151936, k=[16, 3, 9, 1] * 6, d_dtype="fp32", t_dtype="bf16"),
+    dict(vocab=40000, k=list(np.random.default_rng(11).integers(1, 17, size=200)), clip_c=0.05),
+    dict(vocab=1000, k=[16] * 300, d_dtype="fp32", t_dtype="fp32"),
+]
+
+
+@pytest.mark.parametrize("case", STREAM, ids=lambda c: f"V{c['vocab']}_k{len(c['k'])}_{c.get('d_dtype', 'bf16')}")
+def test_streaming_fwd_bwd_shapes(case):
+    b = materialize(custom(**case))
+    nd = b.w.num_draft_rows
+    gsel = sorted(set(np.random.default_rng(5).choice(nd, 6, replace=False)) | {0, nd - 1})
+    _close_to_separate(b, grad_scale=0.5, oracle_grad_rows=gsel)
+
+
+def test_streaming_ragged_vocab_padded_rows():
+    # V = 151937 (not a multiple of 8) with padded leading dimensions, so every row
+    # still starts on the 16-byte grid: the last slice ends in a ragged group
+    w = custom(vocab=151937, k=[5, 12] * 6, ld_d=151944, ld_t=151952)
+    b = materialize(w)
+    f = FusedRun(b, grad_scale=0.25, ld_g=151940)
+    assert f.status_word == 0
+    assert f.canaries_intact() is None, f.canaries_intact()
+    check_verify(f, oracle_argmax_all(b))
+    nd = w.num_draft_rows
+    rows = [0, 7, nd - 1]
+    per, grads = oracle_rows(b, rows, bwd=True, grad_scale=0.25)
+    check_rows(f, per, grads)
+
+
 @pytest.mark.parametrize("misalign", [1, 3])
 def test_unaligned_rows_take_the_separate_path(misalign):
     _close_to_separate(materialize(custom(vocab=5000, k=[3, 8])), misalign=misalign)
