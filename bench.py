@@ -1,7 +1,10 @@
 """Benchmark of the packed verify + OPD-loss pass on GB300.
 
-One step = the whole path over one batch: the fused verify + loss forward
-(row pass K1 + acceptance scan/loss K2) and the backward (K3), through the C ABI.
+One step = the whole path over one batch through the C ABI: verification, the
+clipped reverse-KL + CE loss and its gradient, in one adaflash_opd_loss_fwd_bwd call
+(on this workload: the row pass with the gradient, which reads every logit byte from
+HBM once, then the acceptance scan / loss kernel K2).  The same batch is also timed
+as separate forward (K1 + K2) and backward (K3) calls.
 Default workload: concurrency 128 (V = 151936, bf16 logits, 128 requests with
 k_i from a truncated geometric on 1..16, clip c = 0.5).
 
@@ -38,6 +41,7 @@ LMHEAD_CALLS = 10
 # Sources that decide each kernel's code; a recorded ncu figure is used only while they are unchanged.
 KERNEL_SOURCES = {
     "rowpass_kernel": ("rowpass.cu", "rowstats.cuh", "common.cuh", "kernels.h"),
+    "rowpass_kernel_grad": ("rowpass.cu", "rowstats.cuh", "common.cuh", "kernels.h"),
     "fused_kernel": ("fused.cu", "rowstats.cuh", "common.cuh", "kernels.h"),
     "bwd_kernel": ("backward.cu", "common.cuh", "kernels.h"),
     "lse_rows_kernel": ("sampled.cu", "common.cuh", "kernels.h"),
@@ -189,6 +193,13 @@ def workload_config(w):
     }
 
 
+def single_pass_bytes(w):
+    """adaflash_opd_loss_fwd_bwd on a batch of many rows: every logit byte read once, dz written once."""
+    V = w.vocab
+    bz, bt = w.bytes_per_draft_elem, w.bytes_per_target_elem
+    return (w.num_draft_rows * (bz + bt + 4) + w.num_requests * bt) * V
+
+
 def algorithmic_bytes(w):
     V = w.vocab
     bz, bt = w.bytes_per_draft_elem, w.bytes_per_target_elem
@@ -259,11 +270,12 @@ def run_ours(args):
     grad = torch.empty((Nd, w.vocab), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    fbo = {"grad": grad}
+
     def step():
-        nonlocal out
-        out = af.adaflash_opd_loss_fwd(z, t, tok, doff, w.clip_c, w.ce_weight, out=out, status=status)
-        af.adaflash_opd_loss_bwd(z, t, doff, out["target_argmax"], out["row_stats"], w.clip_c, w.ce_weight,
-                                 grad_scale=1.0 / Nd, out=grad, status=status)
+        nonlocal fbo
+        fbo = af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_scale=1.0 / Nd, out=fbo,
+                                           status=status)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -271,31 +283,43 @@ def run_ours(args):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
 
+    # ---- the timed region: K steps, one adaflash_opd_loss_fwd_bwd call each ----
     K = args.steps
     launches0 = af.adaflash_kernel_launches()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         start.record(stream)
         for i in range(K):
-            e0, e1, e2 = ev[i]
-            e0.record(stream)
-            out = af.adaflash_opd_loss_fwd(z, t, tok, doff, w.clip_c, w.ce_weight, out=out, status=status)
-            e1.record(stream)
-            af.adaflash_opd_loss_bwd(z, t, doff, out["target_argmax"], out["row_stats"], w.clip_c, w.ce_weight,
-                                     grad_scale=1.0 / Nd, out=grad, status=status)
-            e2.record(stream)
+            step()
         stop.record(stream)
         torch.cuda.synchronize()
     barrier()
     launches = af.adaflash_kernel_launches() - launches0
     ms_local = start.elapsed_time(stop)
     ms = max_over_ranks(ms_local, dev if world > 1 else None)
-    fwd_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / K
-    bwd_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / K
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+
+    # the same step as separate forward and backward calls (per-call events)
+    Ks = max(20, K // 2)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(Ks)]
+    for i in range(Ks + 3):
+        if i >= 3:
+            ev[i - 3][0].record(stream)
+        out = af.adaflash_opd_loss_fwd(z, t, tok, doff, w.clip_c, w.ce_weight, out=out, status=status)
+        if i >= 3:
+            ev[i - 3][1].record(stream)
+        af.adaflash_opd_loss_bwd(z, t, doff, out["target_argmax"], out["row_stats"], w.clip_c, w.ce_weight,
+                                 grad_scale=1.0 / Nd, out=grad, status=status)
+        if i >= 3:
+            ev[i - 3][2].record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / Ks
+    bwd_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / Ks
+    sep_ms = sum(e0.elapsed_time(e2) for e0, _, e2 in ev) / Ks
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
 
@@ -310,18 +334,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     fwd_alone_ms = fa.elapsed_time(fb_) / Kf
 
-    # the single-call training step (adaflash_opd_loss_fwd_bwd), calls back to back
-    fbo = af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_scale=1.0 / Nd,
-                                       out={"grad": grad}, status=status)
-    torch.cuda.synchronize()
-    fa2, fb2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    fa2.record(stream)
-    for _ in range(Kf):
-        fbo = af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_scale=1.0 / Nd, out=fbo,
-                                           status=status)
-    fb2.record(stream)
-    torch.cuda.synchronize()
-    fwd_bwd_ms = fa2.elapsed_time(fb2) / Kf
+    fwd_bwd_ms = ms_local / K
 
     # temperature-sampled verification of the same batch (seeded uniforms, T = 0.8), calls back to back
     urng = np.random.default_rng(1000 + rank)
@@ -340,7 +353,7 @@ def run_ours(args):
         raise RuntimeError(f"device status {int(status.item())}")
 
     # cold-HBM per-call times: an L2-sized flush (twice the L2) before every call
-    cold = run_cold(w, dev, af, torch, np, z, t, tok, doff, status, out, grad, stream)
+    cold = run_cold(w, dev, af, torch, np, z, t, tok, doff, status, out, grad, stream, fbo)
 
     # concurrency 1 (one request of 16 draft rows): the step eager and replayed from a CUDA graph
     small = run_small_batch_graph(dev, af, torch, np, make_workload, materialize)
@@ -360,12 +373,14 @@ def run_ours(args):
 
     peak, peak_kind = hbm_peak()
     fb, bb = algorithmic_bytes(w)
+    spb = single_pass_bytes(w)
     traffic = ncu_traffic()
     fwd_gbs = fb / (fwd_ms * 1e-3) / 1e9
     bwd_gbs = bb / (bwd_ms * 1e-3) / 1e9
     fwd_alone_gbs = fb / (fwd_alone_ms * 1e-3) / 1e9
     kernels = {
-        "fwd_pass": {"kernels": "rowpass (K1) + finalize (K2), inside the step (after the previous backward)",
+        "fwd_pass": {"kernels": "rowpass (K1) + finalize (K2), in the separate-call step (after the previous "
+                                "backward)",
                      "ms": fwd_ms, "bytes": fb, "achieved_gbs": fwd_gbs,
                      "frac": fwd_gbs / peak, "rows_per_s": Nd / (fwd_ms * 1e-3)},
         "fwd_alone": {"kernels": "rowpass (K1) + finalize (K2), forward calls back to back", "ms": fwd_alone_ms,
@@ -373,23 +388,32 @@ def run_ours(args):
                       "rows_per_s": Nd / (fwd_alone_ms * 1e-3)},
         "bwd": {"kernels": "bwd (K3)", "ms": bwd_ms, "bytes": bb, "achieved_gbs": bwd_gbs, "frac": bwd_gbs / peak,
                 "rows_per_s": Nd / (bwd_ms * 1e-3)},
-        "fwd_bwd_call": {"kernels": "adaflash_opd_loss_fwd_bwd: K4 (fused, on chip) for batches within one wave of "
-                                    "row units, else K1 + K2 + K3; calls back to back",
-                         "ms": fwd_bwd_ms, "bytes": fb + bb, "achieved_gbs": (fb + bb) / (fwd_bwd_ms * 1e-3) / 1e9,
-                         "frac": (fb + bb) / (fwd_bwd_ms * 1e-3) / 1e9 / peak,
-                         "rows_per_s": Nd / (fwd_bwd_ms * 1e-3)},
+        "fwd_bwd_call": {"kernels": "adaflash_opd_loss_fwd_bwd (the step): the row pass with the gradient (a bulk "
+                                    "launch and a tail launch; each slice read from HBM once, re-read from L2 for "
+                                    "dz) + K2; calls back to back",
+                         "ms": fwd_bwd_ms, "bytes": spb, "achieved_gbs": spb / (fwd_bwd_ms * 1e-3) / 1e9,
+                         "frac": spb / (fwd_bwd_ms * 1e-3) / 1e9 / peak, "rows_per_s": Nd / (fwd_bwd_ms * 1e-3),
+                         "traffic": traffic.get("rowpass_kernel_grad", {}).get("dram_bytes_per_launch")},
+        "step_separate": {"kernels": "adaflash_opd_loss_fwd (K1 + K2) then adaflash_opd_loss_bwd (K3), per-call "
+                                     "events", "ms": sep_ms, "bytes": fb + bb,
+                          "achieved_gbs": (fb + bb) / (sep_ms * 1e-3) / 1e9,
+                          "frac": (fb + bb) / (sep_ms * 1e-3) / 1e9 / peak, "rows_per_s": Nd / (sep_ms * 1e-3)},
         "sampled_verify": {"kernels": f"lse_rows (S1) + accept/draw (S2), T = {SAMPLED_T}, calls back to back",
                            "ms": sampled_ms, "bytes": fb, "achieved_gbs": fb / (sampled_ms * 1e-3) / 1e9,
                            "frac": fb / (sampled_ms * 1e-3) / 1e9 / peak, "rows_per_s": Nd / (sampled_ms * 1e-3),
                            "traffic": _sum_traffic(traffic, ("lse_rows_kernel", "sampled_draw_kernel"))},
     }
-    dom = "bwd" if bwd_ms >= fwd_ms else "fwd_pass"
-    tr_key = "bwd_kernel" if dom == "bwd" else "rowpass_kernel"
-    roofline = {"bound": "hbm", "achieved": kernels[dom]["achieved_gbs"], "peak": peak, "unit": "GB/s",
-                "frac": kernels[dom]["frac"], "traffic": traffic.get(tr_key, {}).get("dram_bytes_per_launch"),
-                "kernel": kernels[dom]["kernels"], "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "algorithmic_bytes_per_launch": kernels[dom]["bytes"]}
+    # The step's dominant kernel is the row pass with the gradient; its time is taken as
+    # the whole call's (the acceptance scan / loss kernel adds a few microseconds).
+    roofline = {"bound": "hbm", "achieved": kernels["fwd_bwd_call"]["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                "frac": kernels["fwd_bwd_call"]["frac"],
+                "traffic": traffic.get("rowpass_kernel_grad", {}).get("dram_bytes_per_launch"),
+                "kernel": "row pass with the gradient (bulk + tail launch) + K2, per adaflash_opd_loss_fwd_bwd call",
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": spb}
+    roofline_bwd = {"bound": "hbm", "achieved": bwd_gbs, "peak": peak, "unit": "GB/s", "frac": bwd_gbs / peak,
+                    "traffic": traffic.get("bwd_kernel", {}).get("dram_bytes_per_launch"),
+                    "kernel": "bwd (K3) in the separate-call step", "algorithmic_bytes_per_launch": bb}
     roofline_lmhead = None
     if lm is not None:
         tpeak, tkind = tensor_peak()
@@ -414,7 +438,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; no datasets or weights)",
-        "config": workload_config(w), "roofline": roofline, "roofline_fwd": roofline_fwd,
+        "config": workload_config(w), "roofline": roofline, "roofline_fwd": roofline_fwd, "roofline_bwd": roofline_bwd,
         "roofline_lmhead": roofline_lmhead, "kernels": kernels, "small_batch": small, "cold": cold,
         "e2e": e2e, "gpu_launches": launches, "clocks": clk.summary(),
         "cpu_baseline": cpu_baseline(b) if world == 1 or rank == 0 else None,
@@ -435,12 +459,20 @@ def tensor_peak():
         return 1900.0, "fallback"
 
 
-def run_cold(w, dev, af, torch, np, z, t, tok, doff, status, out, grad, stream, reps=21):
-    """Forward and backward calls each timed after writing twice the L2 size (cold HBM);
-    median and 10th / 90th percentiles over the reps."""
+def run_cold(w, dev, af, torch, np, z, t, tok, doff, status, out, grad, stream, fbo, reps=21):
+    """The step call, the forward call and the backward call, each timed after writing
+    twice the L2 size (cold HBM); median and 10th / 90th percentiles over the reps."""
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (129 << 20)
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
     Nd = w.num_draft_rows
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for r in range(reps):
+        flush.fill_((r + 7) & 0xff)
+        a, b = evs[r]
+        a.record(stream)
+        af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_scale=1.0 / Nd, out=fbo,
+                                     status=status)
+        b.record(stream)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * reps)]
     for r in range(reps):
         flush.fill_(r & 0xff)
@@ -455,6 +487,7 @@ def run_cold(w, dev, af, torch, np, z, t, tok, doff, status, out, grad, stream, 
                                  grad_scale=1.0 / Nd, out=grad, status=status)
         b.record(stream)
     torch.cuda.synchronize()
+    stp = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
     fwd = sorted(ev[2 * r][0].elapsed_time(ev[2 * r][1]) * 1e3 for r in range(reps))
     bwd = sorted(ev[2 * r + 1][0].elapsed_time(ev[2 * r + 1][1]) * 1e3 for r in range(reps))
     del flush
@@ -463,6 +496,7 @@ def run_cold(w, dev, af, torch, np, z, t, tok, doff, status, out, grad, stream, 
         return xs[min(len(xs) - 1, int(round(f * (len(xs) - 1))))]
 
     return {"flush_bytes": 2 * l2, "reps": reps,
+            "step_us": {"median": q(stp, 0.5), "p10": q(stp, 0.1), "p90": q(stp, 0.9)},
             "fwd_us": {"median": q(fwd, 0.5), "p10": q(fwd, 0.1), "p90": q(fwd, 0.9)},
             "bwd_us": {"median": q(bwd, 0.5), "p10": q(bwd, 0.1), "p90": q(bwd, 0.9)}}
 
@@ -601,10 +635,9 @@ def run_e2e(args, b, w, dev, af, torch, np):
             bf["doff"].copy_(doffh, non_blocking=True)
             copied[k].record(copy_stream)
         comp.wait_event(copied[k])
-        out = af.adaflash_opd_loss_fwd(bf["zv"], bf["tv"], bf["tok"], bf["doff"], w.clip_c, w.ce_weight, out=out,
-                                       status=status)
-        af.adaflash_opd_loss_bwd(bf["zv"], bf["tv"], bf["doff"], out["target_argmax"], out["row_stats"], w.clip_c,
-                                 w.ce_weight, grad_scale=1.0 / Nd, out=grad, status=status)
+        out = af.adaflash_opd_loss_fwd_bwd(bf["zv"], bf["tv"], bf["tok"], bf["doff"], w.clip_c, w.ce_weight,
+                                           grad_scale=1.0 / Nd, out=out if out is not None else {"grad": grad},
+                                           status=status)
         consumed[k].record(comp)
         for key, v in res_h.items():
             v.copy_(out[key], non_blocking=True)

@@ -16,8 +16,8 @@ using namespace adaflash;
 
 namespace {
 
-// adaflash_opd_loss_fwd_bwd on more than a wave of row units: 1 = the single-pass
-// row pass with the gradient, 0 = the forward row pass, then the backward.
+// adaflash_opd_loss_fwd_bwd on more than a wave of row units: 1 = the row pass with
+// the gradient (one pass over HBM), 0 = the forward row pass, then the backward.
 #ifndef ADAFLASH_FWDBWD_STREAM
 #define ADAFLASH_FWDBWD_STREAM 1
 #endif
