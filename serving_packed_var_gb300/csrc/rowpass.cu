@@ -77,6 +77,16 @@ __host__ __device__ constexpr int chunk_of() {
   return DZ::kBytes + DT::kBytes <= 4 ? ADAFLASH_ROWPASS_CHUNK : ADAFLASH_ROWPASS_CHUNK / 2;
 }
 static_assert((ADAFLASH_ROWPASS_CHUNK / 2) % (8 * kConsumers) == 0, "a chunk gives every consumer thread whole groups");
+// With the gradient: L2 priority hints on the two passes' bulk copies (keep, then
+// drop), and the order of the second pass over a slice (1: last chunk first).
+#ifndef ADAFLASH_FB_L2_HINTS
+#define ADAFLASH_FB_L2_HINTS 1
+#endif
+#ifndef ADAFLASH_FB_P2_REVERSE
+#define ADAFLASH_FB_P2_REVERSE 1
+#endif
+constexpr bool kL2Hints = ADAFLASH_FB_L2_HINTS != 0;
+constexpr bool kReverseP2 = ADAFLASH_FB_P2_REVERSE != 0;
 
 }  // namespace
 
@@ -185,8 +195,10 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
         const uint8_t* trow =
             static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(max(U.s, 0)) * P.ld_t * DT::kBytes;
         const int passes = (kGrad && U.pair && !U.bad) ? 2 : 1;
+        const int nch = (body + kChunk - 1) / kChunk;
         for (int pass = 0; pass < passes && !*abort_flag; ++pass) {
-          for (int e0 = 0; e0 < body; e0 += kChunk, ++cc) {
+          for (int ci = 0; ci < nch; ++ci, ++cc) {
+            const int e0 = (pass == 1 && kReverseP2) ? (nch - 1 - ci) * kChunk : ci * kChunk;
             const int st = static_cast<int>(cc % kStages);
             if (cc >= static_cast<uint32_t>(kStages) &&
                 !mbar_wait_bounded(&empty_bar[st], ((cc / kStages) & 1) ^ 1)) {
@@ -200,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
             uint8_t* stage = ring + st * (kStageZ + kStageT);
             const uint8_t* zsrc = zrow + static_cast<int64_t>(v_begin + e0) * DZ::kBytes;
             const uint8_t* tsrc = trow + static_cast<int64_t>(v_begin + e0) * DT::kBytes;
-            if (kGrad && U.pair) {
+            if (kGrad && U.pair && kL2Hints) {
               const uint64_t pol = pass == 0 ? keep : drop;
               bulk_copy_g2s_hint(stage, zsrc, bz, &full_bar[st], pol);
               bulk_copy_g2s_hint(stage + kStageZ, tsrc, bt, &full_bar[st], pol);
@@ -532,7 +544,9 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
           // ---- second pass over the slice (from L2): dz, written once ----
           const RowGrad k = s_grad;
           float* grow = P.grad + static_cast<int64_t>(U.d) * P.ld_g + v_begin;
-          for (int e0 = 0; e0 < body; e0 += kChunk, ++cc) {
+          const int nch = (body + kChunk - 1) / kChunk;
+          for (int ci = 0; ci < nch; ++ci, ++cc) {
+            const int e0 = kReverseP2 ? (nch - 1 - ci) * kChunk : ci * kChunk;
             const int st = static_cast<int>(cc % kStages);
             if (!mbar_wait_bounded(&full_bar[st], (cc / kStages) & 1)) {
               atomicOr(&s_unit_err, 1);
@@ -759,17 +773,29 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   const int split = (units / clusters) * clusters;
   if (!ADAFLASH_ROWPASS_TAIL || units <= clusters || split == units || p.cluster >= kMaxCluster)
     return launch_range<DZ, DT, kFast, kGrad>(p, false, stream);
-  RowPassParams tail = p;
+  const RowPassParams base = p;
   p.unit_end = split;
   cudaError_t e = launch_range<DZ, DT, kFast, kGrad>(p, false, stream);
   if (e != cudaSuccess) return e;
-  tail.unit_begin = split;
-  tail.unit_end = units;
-  tail.wait_prior = 1;
-  tail.cluster = rowpass_cluster_size(p.V, units - split, sm_count());
-  if (tail.cluster < p.cluster) tail.cluster = p.cluster;
-  tail.slice = rowpass_slice(p.V, tail.cluster);
-  return launch_range<DZ, DT, kFast, kGrad>(tail, true, stream);
+  auto launch_tail = [&](int b, int end) {
+    RowPassParams tail = base;
+    tail.unit_begin = b;
+    tail.unit_end = end;
+    tail.wait_prior = 1;
+    tail.cluster = rowpass_cluster_size(p.V, end - b, sm_count());
+    if (tail.cluster < p.cluster) tail.cluster = p.cluster;
+    tail.slice = rowpass_slice(p.V, tail.cluster);
+    return launch_range<DZ, DT, kFast, kGrad>(tail, true, stream);
+  };
+  // With the gradient, leftover paired rows and the cheap target-only rows get their
+  // own launches, so the few expensive rows are split over the larger clusters their
+  // count allows.
+  if (kGrad && p0.mode == kModeFwd && split < p0.N_d && p0.N_d < units) {
+    e = launch_tail(split, p0.N_d);
+    if (e != cudaSuccess) return e;
+    return launch_tail(p0.N_d, units);
+  }
+  return launch_tail(split, units);
 }
 
 #ifndef ADAFLASH_FWDBWD_L2_BUDGET
