@@ -152,12 +152,15 @@ adaflash_status adaflash_opd_loss_bwd(
  * article, "On-Policy Distillation (OPD) for Domain Adaptation"), so the upstream
  * weights are known when the forward runs.  Outputs and arguments are those of
  * adaflash_opd_loss_fwd followed by adaflash_opd_loss_bwd with the same clip_c,
- * ce_weight, grad_row and grad_scale, and so are the values, bit for bit.  When
- * every row of draft_logits, target_logits and grad_draft starts on a 16-byte
- * boundary and a row pair fits in the shared memory of a cluster of at most 8 CTAs,
- * each logit is read from HBM once for both passes (the row pair stays on chip
- * while its statistics are combined, then dz is written from there); otherwise
- * the call runs the separate forward and backward kernels.
+ * ce_weight, grad_row and grad_scale; the integer outputs are equal to theirs and
+ * the float outputs agree to float32 rounding (a row's partial sums may be combined
+ * in another order).  When every row of draft_logits, target_logits and grad_draft
+ * starts on a 16-byte boundary, each logit is read from HBM once for both passes:
+ * for at most one wave of row units with every row pair held on chip (a cluster of
+ * at most 8 CTAs) while its statistics are combined, then dz written from there;
+ * for larger batches by a row pass that reads each slice again, from L2, once the
+ * row's statistics are known.  Rows off that grid take the separate forward and
+ * backward kernels.
  */
 adaflash_status adaflash_opd_loss_fwd_bwd(
     const void* draft_logits, adaflash_dtype d_dtype, int64_t ld_d,
