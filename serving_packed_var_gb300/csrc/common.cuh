@@ -240,6 +240,26 @@ __device__ __forceinline__ void mbar_arrive_remote(uint64_t* local_bar, uint32_t
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
+// Store v (a multiple of 16 bytes, 16-byte aligned) into `local_slot`'s copy in CTA
+// `rank` of the cluster with asynchronous stores that report their bytes as
+// transactions on that CTA's copy of `local_bar`: the receiver, which expects the
+// bytes (mbarrier expect_tx) and waits on its barrier, sees the data with no fence
+// on the sending side.
+template <class T>
+__device__ __forceinline__ void st_async_to_rank(const T& v, T* local_slot, uint64_t* local_bar, uint32_t rank) {
+  static_assert(sizeof(T) % 16 == 0 && alignof(T) >= 16, "whole 16-byte words");
+  uint32_t dst, bar;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(smem_addr(local_slot)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(bar) : "r"(smem_addr(local_bar)), "r"(rank));
+  const uint4* w = reinterpret_cast<const uint4*>(&v);
+#pragma unroll
+  for (int i = 0; i < static_cast<int>(sizeof(T) / 16); ++i)
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     dst + 16 * i),
+                 "r"(w[i].x), "r"(w[i].y), "r"(w[i].z), "r"(w[i].w), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 1000000u) {
   uint32_t ok;
   asm volatile(

@@ -164,8 +164,14 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
       mbar_init(&empty_bar[i], kConsumerWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&part_bar[i], static_cast<uint32_t>(C));
-      mbar_init(&corr_bar[i], static_cast<uint32_t>(C));
+      // One local arrival per phase, made when the barrier is armed with the bytes it
+      // expects (the peers' slices arrive as asynchronous-store transactions).  A
+      // slot is armed for its next use right after its wait, before any peer can send
+      // into it again; here for the first two uses.
+      mbar_init(&part_bar[i], 1);
+      mbar_init(&corr_bar[i], 1);
+      mbar_arrive_expect_tx(&part_bar[i], static_cast<uint32_t>(C * sizeof(SlicePartial)));
+      if (kGrad || rank == 0) mbar_arrive_expect_tx(&corr_bar[i], static_cast<uint32_t>(C * sizeof(SliceCorr)));
     }
     fence_barrier_init();
     s_abort = 0;
@@ -328,8 +334,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
         mine.err = s_unit_err;
         s_unit_err = 0;
         const float own_cmax = mine.cmax;
-        for (int r = 0; r < C; ++r) *map_to_rank(&slots[buf][rank], static_cast<uint32_t>(r)) = mine;
-        for (int r = 0; r < C; ++r) mbar_arrive_remote(&part_bar[buf], static_cast<uint32_t>(r));
+        for (int r = 0; r < C; ++r) st_async_to_rank(mine, &slots[buf][rank], &part_bar[buf], static_cast<uint32_t>(r));
         int werr = 0;
         if (!mbar_wait_cluster_bounded(&part_bar[buf], (it >> 1) & 1)) {
           werr = 1;
@@ -337,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
         }
         SlicePartial all;
         combine_partials(slots[buf], C, all);
+        mbar_arrive_expect_tx(&part_bar[buf], static_cast<uint32_t>(C * sizeof(SlicePartial)));  // armed for unit it + 2
         // The lowest index of the maximum lies in the first group holding it.  With the
         // gradient, a pair row's index is found in the second pass by the thread that
         // holds that group (no re-read here).
@@ -518,8 +524,8 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
         }
         // To rank 0 only; with the gradient, to every CTA (each needs S).
         const int nto = kGrad ? C : 1;
-        for (int r = 0; r < nto; ++r) *map_to_rank(&cslots[cbuf][rank], static_cast<uint32_t>(r)) = mine;
-        for (int r = 0; r < nto; ++r) mbar_arrive_remote(&corr_bar[cbuf], static_cast<uint32_t>(r));
+        for (int r = 0; r < nto; ++r)
+          st_async_to_rank(mine, &cslots[cbuf][rank], &corr_bar[cbuf], static_cast<uint32_t>(r));
         if (kGrad || rank == 0) {
           const bool ok = mbar_wait_cluster_bounded(&corr_bar[cbuf], (pit >> 1) & 1);
           if (!ok) *abort_flag = 1;
@@ -531,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
             nclip_all += cslots[cbuf][r].nclip;
             err_all |= cslots[cbuf][r].err;
           }
+          mbar_arrive_expect_tx(&corr_bar[cbuf], static_cast<uint32_t>(C * sizeof(SliceCorr)));  // armed for pit + 2
           if (rank == 0) finish_row(corr_all, sclip_all, nclip_all, err_all);
           if (kGrad) set_grad(sclip_all);
         }
