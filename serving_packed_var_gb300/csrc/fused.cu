@@ -121,8 +121,12 @@ __global__ void __launch_bounds__(kFThreads, ADAFLASH_FUSED_CTAS_PER_SM) fused_k
   if (tid == 0) {
     mbar_init(&full_bar, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&part_bar[i], static_cast<uint32_t>(C));
-      mbar_init(&corr_bar[i], static_cast<uint32_t>(C));
+      // one local arrival per phase, made when armed with the expected bytes (the
+      // peers' slices arrive as asynchronous-store transactions); re-armed after each wait
+      mbar_init(&part_bar[i], 1);
+      mbar_init(&corr_bar[i], 1);
+      mbar_arrive_expect_tx(&part_bar[i], static_cast<uint32_t>(C * sizeof(SlicePartial)));
+      mbar_arrive_expect_tx(&corr_bar[i], static_cast<uint32_t>(C * sizeof(SliceCorr)));
     }
     fence_barrier_init();
     s_abort = 0;
@@ -215,8 +219,7 @@ __global__ void __launch_bounds__(kFThreads, ADAFLASH_FUSED_CTAS_PER_SM) fused_k
       SlicePartial mine;
       combine_partials(warp_part, kFWarps, mine);
       mine.err = s_abort;
-      for (int r = 0; r < C; ++r) *map_to_rank(&slots[buf][rank], static_cast<uint32_t>(r)) = mine;
-      for (int r = 0; r < C; ++r) mbar_arrive_remote(&part_bar[buf], static_cast<uint32_t>(r));
+      for (int r = 0; r < C; ++r) st_async_to_rank(mine, &slots[buf][rank], &part_bar[buf], static_cast<uint32_t>(r));
       int werr = 0;
       if (!mbar_wait_cluster_bounded(&part_bar[buf], (it >> 1) & 1)) {
         werr = 1;
@@ -224,6 +227,7 @@ __global__ void __launch_bounds__(kFThreads, ADAFLASH_FUSED_CTAS_PER_SM) fused_k
       }
       SlicePartial all;
       combine_partials(slots[buf], C, all);
+      mbar_arrive_expect_tx(&part_bar[buf], static_cast<uint32_t>(C * sizeof(SlicePartial)));  // armed for unit it + 2
       s_mt = all.mt;
       s_bgrp = all.bgrp;
       rc.err = all.err | werr;
@@ -329,8 +333,8 @@ __global__ void __launch_bounds__(kFThreads, ADAFLASH_FUSED_CTAS_PER_SM) fused_k
             mine.nclip += warp_nclip[w];
           }
           // every CTA needs S for its slice of dz: the corrections go to every rank
-          for (int r = 0; r < C; ++r) *map_to_rank(&cslots[cbuf][rank], static_cast<uint32_t>(r)) = mine;
-          for (int r = 0; r < C; ++r) mbar_arrive_remote(&corr_bar[cbuf], static_cast<uint32_t>(r));
+          for (int r = 0; r < C; ++r)
+            st_async_to_rank(mine, &cslots[cbuf][rank], &corr_bar[cbuf], static_cast<uint32_t>(r));
           const bool ok = mbar_wait_cluster_bounded(&corr_bar[cbuf], (pit >> 1) & 1);
           if (!ok) s_abort = 1;
           float corr_all = 0.f, sclip_all = 0.f;
@@ -341,6 +345,7 @@ __global__ void __launch_bounds__(kFThreads, ADAFLASH_FUSED_CTAS_PER_SM) fused_k
             nclip_all += cslots[cbuf][r].nclip;
             err_all |= cslots[cbuf][r].err;
           }
+          mbar_arrive_expect_tx(&corr_bar[cbuf], static_cast<uint32_t>(C * sizeof(SliceCorr)));  // armed for pit + 2
           s_corr_all = corr_all;
           s_sclip_all = sclip_all;
           s_nclip_all = nclip_all;
