@@ -148,6 +148,7 @@ STREAM = [
     dict(vocab=151936, k=[16, 3, 9, 1] * 6, d_dtype="fp32", t_dtype="bf16"),
     dict(vocab=40000, k=list(np.random.default_rng(11).integers(1, 17, size=200)), clip_c=0.05),
     dict(vocab=1000, k=[16] * 300, d_dtype="fp32", t_dtype="fp32"),
+    dict(vocab=151936, k=[16, 5, 11] * 4, d_dtype="fp32", t_dtype="fp32", clip_c=0.2),
 ]
 
 
