@@ -14,8 +14,9 @@
 //                     on max_v (z_v - t_v), the lowest-index argmax of t, and the
 //                     largest group maximum of z each thread sees.
 //
-// Slice results meet over distributed shared memory (remote stores + remote
-// mbarrier arrivals, double-buffered by unit parity).  Every CTA combines them in
+// Slice results meet over distributed shared memory (asynchronous remote stores
+// that complete on the receiver's mbarrier, double-buffered by unit parity).  Every
+// CTA combines them in
 // the same fixed order and gets the row's log-sum-exps, the unclipped reverse KL
 //     KL = sum_v p_v (z_v - t_v) - (lse_z - lse_t),
 // and the bound term_v = p_v r_v <= p_v R, R = max_v(z_v - t_v) - (lse_z - lse_t).
@@ -32,6 +33,10 @@
 // float64 pipe for a whole warp's worth of lanes, and the per-row tail of this
 // kernel runs on a single thread.  The difference of log-sum-exps is taken as
 // (n_t - n_z) ln 2 + ln(S_z / S_t), never as a difference of two large logs.
+//
+// The kGrad instantiation also writes dz: a second pass over each slice, served
+// from L2, once the row's constants and clip corrections are known (see the
+// comment at RowGrad below).
 //
 // Operations: AdaFlash article ("AdaFlash: Adaptive Speculative Decoding with
 // Online Self-Improvement for High-Concurrency LLM Inference"), sections
@@ -155,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
   uint8_t* ring =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
   // One screening code per consumer thread and slot: slot c < #chunks covers the
-  // thread's two groups of ring chunk c, later slots one directly loaded group each.
+  // thread's groups of ring chunk c, later slots one directly loaded group each.
   uint16_t* codes = reinterpret_cast<uint16_t*>(ring + kStages * (kStageZ + kStageT));
 
   if (tid == 0) {
