@@ -648,6 +648,12 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
 #ifndef ADAFLASH_ROWPASS_TAIL
 #define ADAFLASH_ROWPASS_TAIL 1  // the last partial wave of units as a second launch with larger clusters
 #endif
+// Cluster size of a tail launch: 1 = the largest that still holds all of its rows in
+// one wave of resident CTAs, 0 = the row pass's rule (enough CTAs to fill the GPU).
+#ifndef ADAFLASH_ROWPASS_TAIL_ONE_WAVE
+#define ADAFLASH_ROWPASS_TAIL_ONE_WAVE 1
+#endif
+constexpr bool kTailOneWave = ADAFLASH_ROWPASS_TAIL_ONE_WAVE != 0;
 #ifndef ADAFLASH_ROWPASS_SLICE_TARGET
 #define ADAFLASH_ROWPASS_SLICE_TARGET 160000
 #endif
@@ -794,7 +800,15 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
     tail.unit_begin = b;
     tail.unit_end = end;
     tail.wait_prior = 1;
-    tail.cluster = rowpass_cluster_size(p.V, end - b, sm_count());
+    if (kTailOneWave) {
+      // the largest cluster that still fits all of the tail's rows in one wave
+      const long long cap = static_cast<long long>(ADAFLASH_ROWPASS_MINBLOCKS) * sm_count();
+      int c = 1;
+      while (c < kMaxCluster && static_cast<long long>(end - b) * (c + 1) <= cap) ++c;
+      tail.cluster = c;
+    } else {
+      tail.cluster = rowpass_cluster_size(p.V, end - b, sm_count());
+    }
     if (tail.cluster < p.cluster) tail.cluster = p.cluster;
     tail.slice = rowpass_slice(p.V, tail.cluster);
     return launch_range<DZ, DT, kFast, kGrad>(tail, true, stream);
