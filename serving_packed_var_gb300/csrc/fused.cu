@@ -438,7 +438,7 @@ struct FOcc {
   int device;
   int clusters;
 };
-FOcc g_focc[32];
+FOcc g_focc[64];
 int g_focc_n = 0;
 }  // namespace
 
@@ -487,7 +487,7 @@ static int fused_resident_clusters(int C, size_t smem, int num_sms) {
     clusters = num_sms / C;  // one CTA per SM: always resident
     if (clusters < 1) clusters = 1;
   }
-  if (g_focc_n < 32) g_focc[g_focc_n++] = FOcc{reinterpret_cast<const void*>(kern), C, smem, device, clusters};
+  if (g_focc_n < 64) g_focc[g_focc_n++] = FOcc{reinterpret_cast<const void*>(kern), C, smem, device, clusters};
   return clusters;
 }
 
