@@ -160,6 +160,15 @@ def test_streaming_fwd_bwd_shapes(case):
     _close_to_separate(b, grad_scale=0.5, oracle_grad_rows=gsel)
 
 
+def test_streaming_per_row_weights():
+    # more row units than one wave of the on-chip kernel holds: the streaming pass with
+    # an upstream weight per draft row
+    w = custom(vocab=20000, k=[16, 7, 12, 3] * 12, clip_c=0.3)
+    nd = w.num_draft_rows
+    gsel = sorted(set(np.random.default_rng(6).choice(nd, 6, replace=False)) | {0, nd - 1})
+    _close_to_separate(materialize(w), grad_row=np.linspace(-1.5, 2.0, nd), oracle_grad_rows=gsel)
+
+
 def test_streaming_ragged_vocab_padded_rows():
     # V = 151937 (not a multiple of 8) with padded leading dimensions, so every row
     # still starts on the 16-byte grid: the last slice ends in a ragged group
