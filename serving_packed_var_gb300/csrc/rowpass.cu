@@ -55,33 +55,52 @@ namespace adaflash {
 
 namespace {
 
+// CTA shape, ring depth, stage size and resident CTAs per SM (compile-time tuning;
+// the defaults are the measured best on GB300 for bf16 logits).  The forward: two
+// CTAs per SM of 8 consumer warps, each with a 96 KB ring of three 8192-entry
+// stages of z and t.  With the gradient: four CTAs per SM of 4 consumer warps with
+// 48 KB rings of three 4096-entry stages (more CTAs per SM hide the per-row
+// exchanges better; 237 -> 228 us on a 914-row batch at V = 151936).
 #ifndef ADAFLASH_ROWPASS_CONSUMER_WARPS
 #define ADAFLASH_ROWPASS_CONSUMER_WARPS 8
-#endif
-constexpr int kConsumerWarps = ADAFLASH_ROWPASS_CONSUMER_WARPS;
-static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "a power-of-two number of consumer warps");
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
-// Ring depth, stage size and resident CTAs per SM (compile-time tuning; the
-// defaults are the measured best on GB300 for bf16 logits: two CTAs per SM, each
-// with a 96 KB ring of three 8192-entry stages of z and t).
-#ifndef ADAFLASH_ROWPASS_STAGES
-#define ADAFLASH_ROWPASS_STAGES 3
 #endif
 #ifndef ADAFLASH_ROWPASS_MINBLOCKS
 #define ADAFLASH_ROWPASS_MINBLOCKS 2
 #endif
-constexpr int kStages = ADAFLASH_ROWPASS_STAGES;
 #ifndef ADAFLASH_ROWPASS_CHUNK
 #define ADAFLASH_ROWPASS_CHUNK 8192
 #endif
-// Entries of each tensor per stage: ADAFLASH_ROWPASS_CHUNK for two 16-bit inputs,
-// half of it when either input is float32 (the same ring bytes).
-template <class DZ, class DT>
+#ifndef ADAFLASH_FB_CONSUMER_WARPS
+#define ADAFLASH_FB_CONSUMER_WARPS 4
+#endif
+#ifndef ADAFLASH_FB_MINBLOCKS
+#define ADAFLASH_FB_MINBLOCKS 4
+#endif
+#ifndef ADAFLASH_FB_CHUNK
+#define ADAFLASH_FB_CHUNK 4096
+#endif
+#ifndef ADAFLASH_ROWPASS_STAGES
+#define ADAFLASH_ROWPASS_STAGES 3
+#endif
+constexpr int kStages = ADAFLASH_ROWPASS_STAGES;
+
+template <bool kGrad>
+struct RowCfg {
+  static constexpr int kWarps = kGrad ? ADAFLASH_FB_CONSUMER_WARPS : ADAFLASH_ROWPASS_CONSUMER_WARPS;
+  static constexpr int kConsumers = kWarps * 32;
+  static constexpr int kThreads = kConsumers + 32;  // + one producer warp
+  static constexpr int kMinBlocks = kGrad ? ADAFLASH_FB_MINBLOCKS : ADAFLASH_ROWPASS_MINBLOCKS;
+  static constexpr int kChunk = kGrad ? ADAFLASH_FB_CHUNK : ADAFLASH_ROWPASS_CHUNK;
+  static_assert((kWarps & (kWarps - 1)) == 0, "a power-of-two number of consumer warps");
+  static_assert((kChunk / 2) % (8 * kConsumers) == 0, "a chunk gives every consumer thread whole groups");
+};
+
+// Entries of each tensor per stage: the configuration's chunk for two 16-bit
+// inputs, half of it when either input is float32 (the same ring bytes).
+template <class DZ, class DT, bool kGrad>
 __host__ __device__ constexpr int chunk_of() {
-  return DZ::kBytes + DT::kBytes <= 4 ? ADAFLASH_ROWPASS_CHUNK : ADAFLASH_ROWPASS_CHUNK / 2;
+  return DZ::kBytes + DT::kBytes <= 4 ? RowCfg<kGrad>::kChunk : RowCfg<kGrad>::kChunk / 2;
 }
-static_assert((ADAFLASH_ROWPASS_CHUNK / 2) % (8 * kConsumers) == 0, "a chunk gives every consumer thread whole groups");
 // With the gradient: L2 priority hints on the two passes' bulk copies (keep, then
 // drop), and the order of the second pass over a slice (1: last chunk first).
 #ifndef ADAFLASH_FB_L2_HINTS
@@ -124,7 +143,10 @@ __device__ __forceinline__ float grad_of(float z, float t, const RowGrad& k) {
 // with streaming stores.  Every CTA of the cluster gets the corrections (every CTA
 // needs S).
 template <class DZ, class DT, bool kFast, bool kGrad>
-__global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_kernel(const RowPassParams P) {
+__global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBlocks)
+    rowpass_kernel(const RowPassParams P) {
+  constexpr int kConsumerWarps = RowCfg<kGrad>::kWarps;
+  constexpr int kConsumers = RowCfg<kGrad>::kConsumers;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages];
   __shared__ uint64_t empty_bar[kStages];
@@ -152,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, ADAFLASH_ROWPASS_MINBLOCKS) rowpass_
   const int ncl = static_cast<int>(gridDim.x) / C;
   const int num_units = P.unit_end;
 
-  constexpr int kChunk = chunk_of<DZ, DT>();
+  constexpr int kChunk = chunk_of<DZ, DT, kGrad>();
   constexpr int kGroupsPerThread = kChunk / 8 / kConsumers;  // 8-entry groups per consumer thread per chunk
   constexpr int kStageZ = kChunk * DZ::kBytes;
   constexpr int kStageT = kChunk * DT::kBytes;
@@ -699,7 +721,8 @@ static int sm_count() {
 
 template <class DZ, class DT, bool kFast, bool kGrad>
 static size_t rowpass_smem(int slice) {
-  constexpr int kChunk = chunk_of<DZ, DT>();
+  constexpr int kChunk = chunk_of<DZ, DT, kGrad>();
+  constexpr int kConsumers = RowCfg<kGrad>::kConsumers;
   const size_t ring = static_cast<size_t>(kStages) * kChunk * (DZ::kBytes + DT::kBytes);
   // screening codes: per consumer thread one slot per ring chunk (+1 for a ragged
   // tail group) on the bulk-copy path, one per group on the direct-load path
@@ -725,7 +748,7 @@ static int active_clusters(int cluster, size_t smem) {
       return g_occ[i].clusters;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(RowCfg<kGrad>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -757,7 +780,7 @@ static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaS
   cudaLaunchConfig_t cfg = {};
   const int grid_clusters = units < clusters ? units : clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters) * static_cast<unsigned>(p.cluster), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(RowCfg<kGrad>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -802,7 +825,7 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
     tail.wait_prior = 1;
     if (kTailOneWave) {
       // the largest cluster that still fits all of the tail's rows in one wave
-      const long long cap = static_cast<long long>(ADAFLASH_ROWPASS_MINBLOCKS) * sm_count();
+      const long long cap = static_cast<long long>(RowCfg<kGrad>::kMinBlocks) * sm_count();
       int c = 1;
       while (c < kMaxCluster && static_cast<long long>(end - b) * (c + 1) <= cap) ++c;
       tail.cluster = c;
@@ -833,7 +856,7 @@ int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int num_sms) 
   // C rows of row_bytes) fit the L2 budget, so that the second pass over each slice
   // is served from L2.
   int c = rowpass_cluster_size(vocab, units, num_sms);
-  while (c < kMaxCluster && static_cast<long long>(ADAFLASH_ROWPASS_MINBLOCKS) * num_sms / c * row_bytes >
+  while (c < kMaxCluster && static_cast<long long>(RowCfg<true>::kMinBlocks) * num_sms / c * row_bytes >
                                 ADAFLASH_FWDBWD_L2_BUDGET)
     ++c;
   return c;
