@@ -848,7 +848,7 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
 }
 
 #ifndef ADAFLASH_FWDBWD_L2_BUDGET
-#define ADAFLASH_FWDBWD_L2_BUDGET (48ll << 20)  // bytes of rows in flight in the single-pass forward + backward
+#define ADAFLASH_FWDBWD_L2_BUDGET (64ll << 20)  // bytes of rows in flight in the single-pass forward + backward
 #endif
 
 int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int num_sms) {
