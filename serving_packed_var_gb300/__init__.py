@@ -113,10 +113,14 @@ def adaflash_verify_packed(target_logits, draft_tokens, draft_offsets, vocab=Non
     Nd = draft_tokens.numel()
     V = target_logits.shape[1] if vocab is None else vocab
     o = dict(out or {})
-    o.setdefault("target_argmax", _i32(Nd + R, dev))
-    o.setdefault("accept_len", _i32(R, dev))
-    o.setdefault("bonus_token", _i32(R, dev))
-    o.setdefault("accept_rate", _f32(R, dev))
+    if "target_argmax" not in o:
+        o["target_argmax"] = _i32(Nd + R, dev)
+    if "accept_len" not in o:
+        o["accept_len"] = _i32(R, dev)
+    if "bonus_token" not in o:
+        o["bonus_token"] = _i32(R, dev)
+    if "accept_rate" not in o:
+        o["accept_rate"] = _f32(R, dev)
     code = _native.lib().adaflash_verify_packed(
         tp, _dtype_code(target_logits), ldt, draft_tokens.data_ptr(), draft_offsets.data_ptr(), R, Nd, V,
         o["target_argmax"].data_ptr(), o["accept_len"].data_ptr(), o["bonus_token"].data_ptr(),
@@ -138,14 +142,22 @@ def adaflash_opd_loss_fwd(draft_logits, target_logits, draft_tokens, draft_offse
     Nd = draft_tokens.numel()
     V = draft_logits.shape[1] if vocab is None else vocab
     o = dict(out or {})
-    o.setdefault("target_argmax", _i32(Nd + R, dev))
-    o.setdefault("accept_len", _i32(R, dev))
-    o.setdefault("bonus_token", _i32(R, dev))
-    o.setdefault("accept_rate", _f32(R, dev))
-    o.setdefault("kl_row", _f32(Nd, dev))
-    o.setdefault("ce_row", _f32(Nd, dev))
-    o.setdefault("row_stats", torch.empty((Nd, 4), dtype=torch.float32, device=dev))
-    o.setdefault("loss", _f32(1, dev))
+    if "target_argmax" not in o:
+        o["target_argmax"] = _i32(Nd + R, dev)
+    if "accept_len" not in o:
+        o["accept_len"] = _i32(R, dev)
+    if "bonus_token" not in o:
+        o["bonus_token"] = _i32(R, dev)
+    if "accept_rate" not in o:
+        o["accept_rate"] = _f32(R, dev)
+    if "kl_row" not in o:
+        o["kl_row"] = _f32(Nd, dev)
+    if "ce_row" not in o:
+        o["ce_row"] = _f32(Nd, dev)
+    if "row_stats" not in o:
+        o["row_stats"] = torch.empty((Nd, 4), dtype=torch.float32, device=dev)
+    if "loss" not in o:
+        o["loss"] = _f32(1, dev)
     code = _native.lib().adaflash_opd_loss_fwd(
         zp, _dtype_code(draft_logits), ldz, tp, _dtype_code(target_logits), ldt,
         draft_tokens.data_ptr(), draft_offsets.data_ptr(), R, Nd, V, float(clip_c), float(ce_weight),
@@ -190,15 +202,24 @@ def adaflash_opd_loss_fwd_bwd(draft_logits, target_logits, draft_tokens, draft_o
     Nd = draft_tokens.numel()
     V = draft_logits.shape[1] if vocab is None else vocab
     o = dict(out or {})
-    o.setdefault("target_argmax", _i32(Nd + R, dev))
-    o.setdefault("accept_len", _i32(R, dev))
-    o.setdefault("bonus_token", _i32(R, dev))
-    o.setdefault("accept_rate", _f32(R, dev))
-    o.setdefault("kl_row", _f32(Nd, dev))
-    o.setdefault("ce_row", _f32(Nd, dev))
-    o.setdefault("row_stats", torch.empty((Nd, 4), dtype=torch.float32, device=dev))
-    o.setdefault("loss", _f32(1, dev))
-    o.setdefault("grad", torch.empty((Nd, V), dtype=torch.float32, device=dev))
+    if "target_argmax" not in o:
+        o["target_argmax"] = _i32(Nd + R, dev)
+    if "accept_len" not in o:
+        o["accept_len"] = _i32(R, dev)
+    if "bonus_token" not in o:
+        o["bonus_token"] = _i32(R, dev)
+    if "accept_rate" not in o:
+        o["accept_rate"] = _f32(R, dev)
+    if "kl_row" not in o:
+        o["kl_row"] = _f32(Nd, dev)
+    if "ce_row" not in o:
+        o["ce_row"] = _f32(Nd, dev)
+    if "row_stats" not in o:
+        o["row_stats"] = torch.empty((Nd, 4), dtype=torch.float32, device=dev)
+    if "loss" not in o:
+        o["loss"] = _f32(1, dev)
+    if "grad" not in o:
+        o["grad"] = torch.empty((Nd, V), dtype=torch.float32, device=dev)
     gp, ldg = _rows(o["grad"], "grad")
     if o["grad"].dtype != torch.float32:
         raise TypeError("grad must be float32")
@@ -229,10 +250,14 @@ def adaflash_verify_sampled(draft_logits, target_logits, draft_tokens, draft_off
         if u.dtype != torch.float32 or u.numel() != n or not u.is_contiguous():
             raise ValueError(f"{name} must be a contiguous float32 tensor of {n} entries")
     o = dict(out or {})
-    o.setdefault("row_lse", _f32(2 * Nd + R, dev))
-    o.setdefault("accept_len", _i32(R, dev))
-    o.setdefault("next_token", _i32(R, dev))
-    o.setdefault("accept_rate", _f32(R, dev))
+    if "row_lse" not in o:
+        o["row_lse"] = _f32(2 * Nd + R, dev)
+    if "accept_len" not in o:
+        o["accept_len"] = _i32(R, dev)
+    if "next_token" not in o:
+        o["next_token"] = _i32(R, dev)
+    if "accept_rate" not in o:
+        o["accept_rate"] = _f32(R, dev)
     code = _native.lib().adaflash_verify_sampled(
         zp, _dtype_code(draft_logits), ldz, tp, _dtype_code(target_logits), ldt,
         draft_tokens.data_ptr(), draft_offsets.data_ptr(), R, Nd, V, float(temperature),
@@ -286,14 +311,22 @@ def adaflash_lmhead_opd_fwd(draft_hidden, target_hidden, draft_head, target_head
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     o = dict(out or {})
-    o.setdefault("target_argmax", _i32(Nd + R, dev))
-    o.setdefault("accept_len", _i32(R, dev))
-    o.setdefault("bonus_token", _i32(R, dev))
-    o.setdefault("accept_rate", _f32(R, dev))
-    o.setdefault("kl_row", _f32(Nd, dev))
-    o.setdefault("ce_row", _f32(Nd, dev))
-    o.setdefault("row_stats", torch.empty((Nd, 4), dtype=torch.float32, device=dev))
-    o.setdefault("loss", _f32(1, dev))
+    if "target_argmax" not in o:
+        o["target_argmax"] = _i32(Nd + R, dev)
+    if "accept_len" not in o:
+        o["accept_len"] = _i32(R, dev)
+    if "bonus_token" not in o:
+        o["bonus_token"] = _i32(R, dev)
+    if "accept_rate" not in o:
+        o["accept_rate"] = _f32(R, dev)
+    if "kl_row" not in o:
+        o["kl_row"] = _f32(Nd, dev)
+    if "ce_row" not in o:
+        o["ce_row"] = _f32(Nd, dev)
+    if "row_stats" not in o:
+        o["row_stats"] = torch.empty((Nd, 4), dtype=torch.float32, device=dev)
+    if "loss" not in o:
+        o["loss"] = _f32(1, dev)
     code = _native.lib().adaflash_lmhead_opd_fwd(
         hdp, ldhd, htp, ldht, wdp, ldwd, wtp, ldwt, H, draft_tokens.data_ptr(), draft_offsets.data_ptr(), R, Nd, V,
         float(clip_c), float(ce_weight), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
