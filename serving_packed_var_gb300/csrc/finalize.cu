@@ -24,6 +24,9 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
   // Launched as a programmatic dependent of the row pass: wait until its writes
   // (target_argmax, kl_row, ce_row) are complete and visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The next call's row pass may be scheduled now; it waits for this grid's
+  // completion before touching global memory.
+  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * kFinThreads + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * kFinThreads) >> 5;

@@ -162,9 +162,6 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
   __shared__ int s_abort;
   __shared__ int s_unit_err;
 
-  // The acceptance scan / loss kernel that follows may be scheduled now; it waits
-  // for this grid's completion before reading what this grid writes.
-  asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -206,6 +203,13 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
   }
   __syncthreads();
   cluster_sync_all();  // every CTA's barriers exist before any remote arrival
+
+  // A bulk launch is a programmatic dependent of whatever the stream ran before it:
+  // nothing in global memory is touched before that grid has completed.  Only then
+  // may the kernels that follow (a tail launch, the acceptance scan / loss kernel)
+  // be scheduled; they wait for this grid before reading what it writes.
+  if (!P.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
 
   volatile int* abort_flag = &s_abort;
 
@@ -813,10 +817,10 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   const int clusters = active_clusters<DZ, DT, kFast, kGrad>(p.cluster, rowpass_smem<DZ, DT, kFast, kGrad>(p.slice));
   const int split = (units / clusters) * clusters;
   if (!ADAFLASH_ROWPASS_TAIL || units <= clusters || split == units || p.cluster >= kMaxCluster)
-    return launch_range<DZ, DT, kFast, kGrad>(p, false, stream);
+    return launch_range<DZ, DT, kFast, kGrad>(p, true, stream);
   const RowPassParams base = p;
   p.unit_end = split;
-  cudaError_t e = launch_range<DZ, DT, kFast, kGrad>(p, false, stream);
+  cudaError_t e = launch_range<DZ, DT, kFast, kGrad>(p, true, stream);
   if (e != cudaSuccess) return e;
   auto launch_tail = [&](int b, int end) {
     RowPassParams tail = base;
