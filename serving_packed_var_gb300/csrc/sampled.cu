@@ -244,7 +244,10 @@ template <class DZ, class DT>
 __global__ void __launch_bounds__(kLseThreads, ADAFLASH_LSE_MINBLOCKS) lse_rows_kernel(const SampledParams P, int C) {
   __shared__ float red[64];
   __shared__ float part[2 * kLseMaxCluster];
-  // S2 may be scheduled as soon as every S1 CTA is running; it waits for S1's results.
+  // S1 is a programmatic dependent of whatever the stream ran before it: nothing in
+  // global memory is touched before that grid has completed.  Then S2 may be
+  // scheduled; it waits for S1's results.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = static_cast<int>(blockIdx.x) / C;
   const int rank = static_cast<int>(blockIdx.x) % C;  // == %cluster_ctarank for a 1-D cluster of C
@@ -318,6 +321,8 @@ __global__ void __launch_bounds__(kDrawThreads, ADAFLASH_DRAW_MINBLOCKS) sampled
   }
   const float w = fminf(fmaxf(__ldg(P.u_sample + i), 0.f), 1.f);  // NaN -> 0
   asm volatile("griddepcontrol.wait;" ::: "memory");  // row_lse comes from S1
+  // the next call's S1 may be scheduled now; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 0) {
     if (!ok) {
       if (lane == 0) {
@@ -566,13 +571,15 @@ static cudaError_t launch_sampled_t(const SampledParams& p, int num_sms, cudaStr
     cfg.gridDim = dim3(static_cast<unsigned>(rows * C));
     cfg.blockDim = dim3(kLseThreads);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(C);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     count_launch();
     const cudaError_t e = cudaLaunchKernelEx(&cfg, lse_rows_kernel<DZ, DT>, p, C);
     if (e != cudaSuccess) return e;
