@@ -400,9 +400,9 @@ def run_ours(args):
                       "rows_per_s": Nd / (fwd_alone_ms * 1e-3)},
         "bwd": {"kernels": "bwd (K3)", "ms": bwd_ms, "bytes": bb, "achieved_gbs": bwd_gbs, "frac": bwd_gbs / peak,
                 "rows_per_s": Nd / (bwd_ms * 1e-3)},
-        "fwd_bwd_call": {"kernels": "adaflash_opd_loss_fwd_bwd (the step): the row pass with the gradient (a bulk "
-                                    "launch and a tail launch; each slice read from HBM once, re-read from L2 for "
-                                    "dz) + K2; calls back to back",
+        "fwd_bwd_call": {"kernels": "adaflash_opd_loss_fwd_bwd (the step): the row pass with the gradient (one "
+                                    "launch on this batch; each slice read from HBM once, re-read from L2 for dz) "
+                                    "+ K2; calls back to back",
                          "ms": fwd_bwd_ms, "bytes": spb, "achieved_gbs": spb / (fwd_bwd_ms * 1e-3) / 1e9,
                          "frac": spb / (fwd_bwd_ms * 1e-3) / 1e9 / peak, "rows_per_s": Nd / (fwd_bwd_ms * 1e-3),
                          "traffic": traffic.get("rowpass_kernel_grad", {}).get("dram_bytes_per_launch")},
@@ -424,7 +424,7 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": kernels["fwd_bwd_call"]["achieved_gbs"], "peak": peak, "unit": "GB/s",
                 "frac": kernels["fwd_bwd_call"]["frac"],
                 "traffic": traffic.get("rowpass_kernel_grad", {}).get("dram_bytes_per_launch"),
-                "kernel": "row pass with the gradient (bulk + tail launch) + K2, per adaflash_opd_loss_fwd_bwd call",
+                "kernel": "row pass with the gradient (one launch on this batch) + K2, per adaflash_opd_loss_fwd_bwd call",
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s", "algorithmic_bytes_per_launch": spb}
     roofline_bwd = {"bound": "hbm", "achieved": bwd_gbs, "peak": peak, "unit": "GB/s", "frac": bwd_gbs / peak,

@@ -816,7 +816,10 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   p.wait_prior = 0;
   const int clusters = active_clusters<DZ, DT, kFast, kGrad>(p.cluster, rowpass_smem<DZ, DT, kFast, kGrad>(p.slice));
   const int split = (units / clusters) * clusters;
-  if (!ADAFLASH_ROWPASS_TAIL || units <= clusters || split == units || p.cluster >= kMaxCluster)
+  // With the gradient, a last partial wave of target-only rows (cheap: no second pass)
+  // stays in the one launch rather than costing a launch of its own.
+  if (!ADAFLASH_ROWPASS_TAIL || units <= clusters || split == units || p.cluster >= kMaxCluster ||
+      (kGrad && p0.mode == kModeFwd && split >= p0.N_d))
     return launch_range<DZ, DT, kFast, kGrad>(p, true, stream);
   const RowPassParams base = p;
   p.unit_end = split;
