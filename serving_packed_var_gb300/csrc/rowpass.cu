@@ -803,9 +803,11 @@ static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaS
 // Whole waves of units run at the requested cluster size; when the units do not
 // fill the last wave, the remainder (the last rows, and the cheap target-only
 // rows) runs as a second launch with larger clusters, so its rows are split
-// over more CTAs instead of leaving a few CTAs to finish whole rows alone.  The
-// second launch starts as CTAs of the first retire (programmatic launch) and
-// completes only after the first.
+// over more CTAs instead of leaving a few CTAs to finish whole rows alone (with
+// the gradient, a remainder of target-only rows only stays in the first launch).
+// Every launch is programmatic: the first one waits for the stream's previous
+// kernel before touching global memory; a second one starts as CTAs of the first
+// retire and completes only after the first.
 template <class DZ, class DT, bool kFast, bool kGrad = false>
 static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   const int units = (p0.mode == kModeVerify) ? p0.N_t : (p0.N_d + p0.R);
