@@ -299,3 +299,96 @@ def test_loss_is_mean_over_draft_rows():
     per2, loss2 = oracle.opd_loss_fwd(dr, tr, doff2, 1.0)
     assert abs(loss1 - loss2) < 1e-14
     assert abs(loss1 * 5 - sum(per[d]["kl"] + per[d]["ce"] for d in range(5))) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# the packed batch walk of the forward and the gradient
+# ---------------------------------------------------------------------------
+
+def _packed_blocks(ks, V, rng):
+    """Per-request blocks (k_i draft rows, k_i + 1 target rows) with some clipped terms."""
+    blocks = []
+    for k in ks:
+        D = rng.normal(0, 2, size=(k, V))
+        T = rng.normal(0, 2, size=(k + 1, V))
+        D[:, :3] += 3.0
+        T[:, :3] -= 3.0
+        blocks.append((D, T))
+    return blocks
+
+
+def _blocks_objective(blocks, g, c, beta):
+    """J = sum over requests i and positions j < k_i of g * loss_row(D_i[j], T_i[j]).
+
+    Written from the blocks themselves (position j of a request pairs its j-th draft row
+    with its j-th target row), not through the packed offsets the oracle walks."""
+    total, d = 0.0, 0
+    for D, T in blocks:
+        for j in range(len(D)):
+            total += g[d] * oracle.row_forward(D[j], T[j], c, beta)["loss_row"]
+            d += 1
+    return total
+
+
+def test_packed_walk_forward_and_gradient_against_the_block_objective():
+    """opd_loss_fwd's batch loss and opd_loss_bwd's packed gradient on three requests of
+    k = {4, 1, 3} with per-row upstream weights, against the objective built from the
+    request blocks and its central differences.  Pairing draft row d with target row d
+    (instead of d + i), or weighting by request instead of by row, fails here."""
+    rng = np.random.default_rng(2024)
+    V, ks, c, beta = 20, [4, 1, 3], 0.35, 0.7
+    blocks = _packed_blocks(ks, V, rng)
+    draft = np.concatenate([D for D, _ in blocks])
+    target = np.concatenate([T for _, T in blocks])
+    doff = np.array([0, 4, 5, 8])
+    Nd = 8
+    g = rng.uniform(0.5, 2.0, size=Nd)
+
+    # the forward's batch loss is the unweighted objective over N_d
+    _, loss = oracle.opd_loss_fwd(lambda d: draft[d], lambda s: target[s], doff, c, beta)
+    assert abs(loss - _blocks_objective(blocks, np.ones(Nd), c, beta) / Nd) < 1e-13
+
+    grad = oracle.opd_loss_bwd(lambda d: draft[d], lambda s: target[s], doff, c, beta, grad_row=g)
+    assert sorted(grad) == list(range(Nd))
+    h, checked, clipped = 1e-6, 0, 0
+    d = 0
+    for i, (D, T) in enumerate(blocks):
+        for j in range(len(D)):
+            _, _, term = clipped_reverse_kl_terms(D[j], T[j])
+            clipped += int(np.count_nonzero(term > c))
+            if np.any(np.abs(term - c) < 1e-3):
+                d += 1
+                continue  # the clip's kink is too close for a central difference
+            for u in range(V):
+                Dp = [(Dk.copy(), Tk) for Dk, Tk in blocks]
+                Dm = [(Dk.copy(), Tk) for Dk, Tk in blocks]
+                Dp[i][0][j, u] += h
+                Dm[i][0][j, u] -= h
+                fd = (_blocks_objective(Dp, g, c, beta) - _blocks_objective(Dm, g, c, beta)) / (2 * h)
+                assert abs(fd - grad[d][u]) <= 1e-6 + 1e-4 * abs(fd), (i, j, u, fd, grad[d][u])
+            checked += 1
+            d += 1
+    assert checked >= 6 and clipped > 0
+
+
+def test_packed_gradient_scalar_weight_is_the_mean_loss_gradient():
+    """grad_scale = 1 / N_d gives the gradient of opd_loss_fwd's mean loss (central differences
+    through the packed forward itself, on a request of k = 1 between two longer ones)."""
+    rng = np.random.default_rng(99)
+    V, ks, c, beta = 12, [3, 1, 2], 0.5, 1.0
+    blocks = _packed_blocks(ks, V, rng)
+    draft = np.concatenate([D for D, _ in blocks])
+    target = np.concatenate([T for _, T in blocks])
+    doff = np.array([0, 3, 4, 6])
+    Nd = 6
+    grad = oracle.opd_loss_bwd(lambda d: draft[d], lambda s: target[s], doff, c, beta, grad_scale=1.0 / Nd)
+    h = 1e-6
+    for d in (0, 3, 5):
+        for u in range(V):
+            zp, zm = draft.copy(), draft.copy()
+            zp[d, u] += h
+            zm[d, u] -= h
+            lp = oracle.opd_loss_fwd(lambda r: zp[r], lambda s: target[s], doff, c, beta)[1]
+            lm = oracle.opd_loss_fwd(lambda r: zm[r], lambda s: target[s], doff, c, beta)[1]
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - grad[d][u]) <= 1e-7 + 1e-4 * abs(fd), (d, u, fd, grad[d][u])
