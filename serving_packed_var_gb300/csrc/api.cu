@@ -144,7 +144,7 @@ adaflash_status adaflash_verify_packed(const void* target_logits, adaflash_dtype
   p.target_argmax = target_argmax;
   p.status = d_status;
   // Target-only units read no draft row; the draft dtype only sizes the ring.
-  ADAFLASH_CUDA(launch_rowpass(p, 1, t_dtype, rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)), s));
+  ADAFLASH_CUDA(launch_rowpass(p, 1, t_dtype, s));
 
   FinalizeParams f = {};
   f.tokens = draft_tokens;
@@ -203,9 +203,7 @@ adaflash_status adaflash_opd_loss_fwd(const void* draft_logits, adaflash_dtype d
   p.ce_row = ce_row;
   p.row_stats = row_stats;
   p.status = d_status;
-  const bool fast = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
-                    rows_16b(target_logits, ld_t, dtype_bytes(t_dtype));
-  ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype, fast, s));
+  ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype, s));
 
   FinalizeParams f = {};
   f.tokens = draft_tokens;
@@ -265,9 +263,7 @@ adaflash_status adaflash_opd_loss_bwd(const void* draft_logits, adaflash_dtype d
   p.ld_g = ld_g;
   p.chunks_per_row = (vocab + kBwdChunk - 1) / kBwdChunk;
   p.status = d_status;
-  const bool fast = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
-                    rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)) && rows_16b(grad_draft, ld_g, 4);
-  ADAFLASH_CUDA(launch_bwd(p, d_dtype, t_dtype, fast, s));
+  ADAFLASH_CUDA(launch_bwd(p, d_dtype, t_dtype, s));
   return ADAFLASH_OK;
 }
 
@@ -319,27 +315,26 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
   p.grad_scale = grad_scale;
   p.grad = grad_draft;
   p.ld_g = ld_g;
-  const bool fast = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
-                    rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)) && rows_16b(grad_draft, ld_g, 4);
-  const bool fused = fast && num_draft_rows + num_requests <= fused_max_units(vocab, d_dtype, t_dtype, num_sms());
-  const bool stream_grad = fast && !fused && kFwdBwdStream;
+  // The on-chip fused kernel holds whole row pairs in shared memory (rows on the
+  // 16-byte grid, at most one wave of row units); otherwise the row pass with the
+  // gradient, which reads the logits from HBM once and writes dz from a second pass
+  // over each slice served by L2 (any element-aligned rows).
+  const bool aligned16 = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
+                         rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)) && rows_16b(grad_draft, ld_g, 4);
+  const bool fused = aligned16 && num_draft_rows + num_requests <= fused_max_units(vocab, d_dtype, t_dtype, num_sms());
+  const bool stream_grad = !fused && kFwdBwdStream;
   if (fused) {
     ADAFLASH_CUDA(launch_fused(p, d_dtype, t_dtype, num_sms(), s));
   } else if (stream_grad) {
-    // more than a wave of row units: one streaming pass per row slice that reads the
-    // logits from HBM once and writes dz from a second pass served by L2
     const int row_bytes = vocab * (dtype_bytes(d_dtype) + dtype_bytes(t_dtype));
     p.cluster = rowpass_grad_cluster_size(vocab, p.N_d + p.R, row_bytes, num_sms());
     p.slice = rowpass_slice(vocab, p.cluster);
     ADAFLASH_CUDA(launch_rowpass_grad(p, d_dtype, t_dtype, s));
   } else {
-    // rows off the 16-byte grid: the streaming forward, then the streaming backward
+    // the streaming forward, then the streaming backward
     p.cluster = rowpass_cluster_size(vocab, p.N_d + p.R, num_sms());
     p.slice = rowpass_slice(vocab, p.cluster);
-    ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype,
-                                 rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
-                                     rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)),
-                                 s));
+    ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype, s));
   }
 
   FinalizeParams f = {};
@@ -380,7 +375,7 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
     b.ld_g = ld_g;
     b.chunks_per_row = (vocab + kBwdChunk - 1) / kBwdChunk;
     b.status = d_status;
-    ADAFLASH_CUDA(launch_bwd(b, d_dtype, t_dtype, fast, s));
+    ADAFLASH_CUDA(launch_bwd(b, d_dtype, t_dtype, s));
   }
   return ADAFLASH_OK;
 }

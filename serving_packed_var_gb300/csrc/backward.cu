@@ -42,28 +42,16 @@ __device__ __forceinline__ float grad_entry(float z, float t, const RowCoef& k) 
   return __fmul_rn(__fmul_rn(p, inner), k.g);
 }
 
-template <class DT>
-__device__ __forceinline__ void load8_vec(const uint8_t* row, int64_t v0, float x[8]);
-
-template <>
-__device__ __forceinline__ void load8_vec<BF16>(const uint8_t* row, int64_t v0, float x[8]) {
-  const uint4 q = __ldg(reinterpret_cast<const uint4*>(row + v0 * 2));
-  x[0] = bf16_lo(q.x); x[1] = bf16_hi(q.x);
-  x[2] = bf16_lo(q.y); x[3] = bf16_hi(q.y);
-  x[4] = bf16_lo(q.z); x[5] = bf16_hi(q.z);
-  x[6] = bf16_lo(q.w); x[7] = bf16_hi(q.w);
-}
-
-template <>
-__device__ __forceinline__ void load8_vec<F32>(const uint8_t* row, int64_t v0, float x[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(row + v0 * 4));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(row + v0 * 4 + 16));
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
 }  // namespace
 
-template <class DZ, class DT, bool kFast>
+// Rows need not start on the 16-byte grid: a row's vocabulary follows its target
+// row's grid (the head, the first H < 8 entries before the target row's first
+// 16-byte boundary, goes through element loads in the CTA of chunk 0; chunk c holds
+// body entries [H + c * kBwdChunk, ...)).  Target groups are then 16-byte words; the
+// draft row's groups sit 2 zs2 bytes past a boundary and are read with aligned loads
+// at that shift (one loop instance per shift); dz is stored at the gradient row's
+// own word offset.
+template <class DZ, class DT>
 __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams P) {
   __shared__ RowCoef s_coef;
   __shared__ int s_ok;
@@ -109,63 +97,64 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams P) {
   const uint8_t* zrow = static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(d) * P.ld_z * DZ::kBytes;
   const uint8_t* trow = static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(s_trow) * P.ld_t * DT::kBytes;
   float* grow = P.grad + static_cast<int64_t>(d) * P.ld_g;
+  const RowGeom G = row_geom<DZ, DT>(zrow, trow, P.V);
 
-  const int v_begin = chunk * kBwdChunk;
-  const int v_end = min(P.V, v_begin + kBwdChunk);
+  const int b_begin = chunk * kBwdChunk;  // in the body
+  const int b_end = min(P.V - G.H, b_begin + kBwdChunk);
+  const int nb = max(0, b_end - b_begin);
+  const int body = nb & ~7;
+  float* gbody = grow + G.H + b_begin;
+  const int gq = static_cast<int>((reinterpret_cast<uintptr_t>(gbody) >> 2) & 3u);
+  const uint32_t* tw = reinterpret_cast<const uint32_t*>(G.tb + static_cast<int64_t>(b_begin) * DT::kBytes);
+  const uint8_t* zb = G.zb + static_cast<int64_t>(b_begin) * DZ::kBytes;
 
-  if (kFast) {
-    const int body = (v_end - v_begin) & ~7;
+  dispatch_shift<DZ>(G.zs2, [&](auto zs_c) {
+    constexpr int ZS = decltype(zs_c)::value;
+    const uint32_t* zw = reinterpret_cast<const uint32_t*>(zb - 2 * ZS);  // the 16-byte boundary below
 #pragma unroll
     for (int j = 0; j < kPerThread / 8; ++j) {
       const int off = (j * kBwdThreads + static_cast<int>(threadIdx.x)) * 8;
       if (off < body) {
-        const int64_t v0 = v_begin + off;
         float z[8], t[8], out[8];
-        load8_vec<DZ>(zrow, v0, z);
-        load8_vec<DT>(trow, v0, t);
+        load8_shifted<DZ, ZS, true>(zw + off * DZ::kBytes / 4, z);
+        load8_shifted<DT, 0, true>(tw + off * DT::kBytes / 4, t);
 #pragma unroll
         for (int e = 0; e < 8; ++e) out[e] = grad_entry(z[e], t[e], k);
-        float4* dst = reinterpret_cast<float4*>(grow + v0);
-        __stcs(dst, make_float4(out[0], out[1], out[2], out[3]));
-        __stcs(dst + 1, make_float4(out[4], out[5], out[6], out[7]));
+        store8_stream(gbody + off, gq, out);
       }
     }
-    for (int v = v_begin + body + static_cast<int>(threadIdx.x); v < v_end; v += kBwdThreads)
+  });
+  // the ragged end of the chunk and, in chunk 0, the row's head: element loads
+  for (int v = G.H + b_begin + body + static_cast<int>(threadIdx.x); v < G.H + b_end; v += kBwdThreads)
+    grow[v] = grad_entry(DZ::load(zrow, v), DT::load(trow, v), k);
+  if (chunk == 0)
+    for (int v = static_cast<int>(threadIdx.x); v < G.H; v += kBwdThreads)
       grow[v] = grad_entry(DZ::load(zrow, v), DT::load(trow, v), k);
-  } else {
-    for (int v = v_begin + static_cast<int>(threadIdx.x); v < v_end; v += kBwdThreads)
-      __stcs(grow + v, grad_entry(DZ::load(zrow, v), DT::load(trow, v), k));
-  }
   __syncthreads();
   // The hard-label term's -beta*g at the target argmax (written after the row's
-  // stores above by the thread that owns that chunk).
-  if (threadIdx.x == 0 && k.a >= v_begin && k.a < v_end) {
+  // stores above by the CTA that holds that entry).
+  const bool owns = (k.a >= G.H + b_begin && k.a < G.H + b_end) || (chunk == 0 && k.a < G.H);
+  if (threadIdx.x == 0 && owns) {
     const float base = grad_entry(DZ::load(zrow, k.a), DT::load(trow, k.a), k);
     grow[k.a] = __fsub_rn(base, __fmul_rn(P.ce_weight, k.g));
   }
 }
 
-template <class DZ, class DT, bool kFast>
+template <class DZ, class DT>
 static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t s) {
   const long long blocks = static_cast<long long>(p.N_d) * p.chunks_per_row;
   if (blocks <= 0) return cudaSuccess;
   count_launch();
-  bwd_kernel<DZ, DT, kFast><<<static_cast<unsigned>(blocks), kBwdThreads, 0, s>>>(p);
+  bwd_kernel<DZ, DT><<<static_cast<unsigned>(blocks), kBwdThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s) {
+cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, cudaStream_t s) {
   const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
-  if (fast) {
-    if (zb && tb) return launch_bwd_t<BF16, BF16, true>(p, s);
-    if (!zb && tb) return launch_bwd_t<F32, BF16, true>(p, s);
-    if (zb && !tb) return launch_bwd_t<BF16, F32, true>(p, s);
-    return launch_bwd_t<F32, F32, true>(p, s);
-  }
-  if (zb && tb) return launch_bwd_t<BF16, BF16, false>(p, s);
-  if (!zb && tb) return launch_bwd_t<F32, BF16, false>(p, s);
-  if (zb && !tb) return launch_bwd_t<BF16, F32, false>(p, s);
-  return launch_bwd_t<F32, F32, false>(p, s);
+  if (zb && tb) return launch_bwd_t<BF16, BF16>(p, s);
+  if (!zb && tb) return launch_bwd_t<F32, BF16>(p, s);
+  if (zb && !tb) return launch_bwd_t<BF16, F32>(p, s);
+  return launch_bwd_t<F32, F32>(p, s);
 }
 
 }  // namespace adaflash

@@ -339,3 +339,166 @@ __device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
 }
 
 }  // namespace adaflash
+
+namespace adaflash {
+
+// ---------------------------------------------------------------------------
+// rows off the 16-byte grid
+// ---------------------------------------------------------------------------
+// A compile-time integer (a row's byte shift against the 16-byte grid, picked per
+// row by a uniform switch, so each shift gets its own straight-line loads).
+template <int N>
+struct IntC {
+  static constexpr int value = N;
+};
+
+// Words base[P .. P+N) of a 16-byte aligned array, each access the widest aligned
+// one (128, 64 or 32 bits): a run that starts P words past a 16-byte boundary.
+template <int P, int N>
+__device__ __forceinline__ void lds_words(const uint32_t* base, uint32_t* w) {
+  if constexpr (N > 0) {
+    if constexpr (P % 4 == 0 && N >= 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(base + P);
+      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+      lds_words<P + 4, N - 4>(base, w + 4);
+    } else if constexpr (P % 2 == 0 && N >= 2) {
+      const uint2 v = *reinterpret_cast<const uint2*>(base + P);
+      w[0] = v.x; w[1] = v.y;
+      lds_words<P + 2, N - 2>(base, w + 2);
+    } else {
+      w[0] = base[P];
+      lds_words<P + 1, N - 1>(base, w + 1);
+    }
+  }
+}
+
+// The same from global memory through the read-only path.
+template <int P, int N>
+__device__ __forceinline__ void ldg_words(const uint32_t* base, uint32_t* w) {
+  if constexpr (N > 0) {
+    if constexpr (P % 4 == 0 && N >= 4) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + P));
+      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+      ldg_words<P + 4, N - 4>(base, w + 4);
+    } else if constexpr (P % 2 == 0 && N >= 2) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(base + P));
+      w[0] = v.x; w[1] = v.y;
+      ldg_words<P + 2, N - 2>(base, w + 2);
+    } else {
+      w[0] = __ldg(base + P);
+      ldg_words<P + 1, N - 1>(base, w + 1);
+    }
+  }
+}
+
+// Streaming stores of x[0 .. N) to base[P .. P+N) (base 16-byte aligned), each the
+// widest aligned store.
+template <int P, int N>
+__device__ __forceinline__ void stcs_words(float* base, const float* x) {
+  if constexpr (N > 0) {
+    if constexpr (P % 4 == 0 && N >= 4) {
+      __stcs(reinterpret_cast<float4*>(base + P), make_float4(x[0], x[1], x[2], x[3]));
+      stcs_words<P + 4, N - 4>(base, x + 4);
+    } else if constexpr (P % 2 == 0 && N >= 2) {
+      __stcs(reinterpret_cast<float2*>(base + P), make_float2(x[0], x[1]));
+      stcs_words<P + 2, N - 2>(base, x + 2);
+    } else {
+      __stcs(base + P, x[0]);
+      stcs_words<P + 1, N - 1>(base, x + 1);
+    }
+  }
+}
+
+// Eight float32 results to dst (4-byte aligned, q = (dst / 4) mod 4 words past a
+// 16-byte boundary; q is uniform across a row, so the branch does not diverge).
+__device__ __forceinline__ void store8_stream(float* dst, int q, const float x[8]) {
+  float* base = dst - q;
+  switch (q) {
+    case 1: stcs_words<1, 8>(base, x); break;
+    case 2: stcs_words<2, 8>(base, x); break;
+    case 3: stcs_words<3, 8>(base, x); break;
+    default: stcs_words<0, 8>(base, x); break;
+  }
+}
+
+// Eight entries of a row whose group starts ZS two-byte units past a 16-byte
+// boundary: words are read with aligned loads (lds_words / ldg_words, picked by
+// kGlobal) from `base` (the 16-byte aligned address at or below the group), then
+// widened.  ZS is even for float32 rows.  A bfloat16 group at an odd ZS straddles
+// five words: its entries are the upper half of word i and the lower half of
+// word i + 1.
+template <class DT, int ZS, bool kGlobal>
+__device__ __forceinline__ void load8_shifted(const uint32_t* base, float x[8]) {
+  if constexpr (DT::kBytes == 4) {
+    static_assert(ZS % 2 == 0, "float32 rows are 4-byte aligned");
+    uint32_t w[8];
+    if constexpr (kGlobal) ldg_words<ZS / 2, 8>(base, w); else lds_words<ZS / 2, 8>(base, w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(w[i]);
+  } else if constexpr (ZS % 2 == 0) {
+    uint32_t w[4];
+    if constexpr (kGlobal) ldg_words<ZS / 2, 4>(base, w); else lds_words<ZS / 2, 4>(base, w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16_lo(w[i]);
+      x[2 * i + 1] = bf16_hi(w[i]);
+    }
+  } else {
+    uint32_t w[5];
+    if constexpr (kGlobal) ldg_words<(ZS - 1) / 2, 5>(base, w); else lds_words<(ZS - 1) / 2, 5>(base, w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16_hi(w[i]);
+      x[2 * i + 1] = bf16_lo(w[i + 1]);
+    }
+  }
+}
+
+// Call f(IntC<zs2>{}) for a row's shift zs2 (in two-byte units, 0..7; only even
+// shifts occur for float32 rows, so only those are instantiated).
+template <class DT, class F>
+__device__ __forceinline__ void dispatch_shift(int zs2, F&& f) {
+  if constexpr (DT::kBytes == 4) {
+    switch (zs2) {
+      case 2: f(IntC<2>{}); break;
+      case 4: f(IntC<4>{}); break;
+      case 6: f(IntC<6>{}); break;
+      default: f(IntC<0>{}); break;
+    }
+  } else {
+    switch (zs2) {
+      case 1: f(IntC<1>{}); break;
+      case 2: f(IntC<2>{}); break;
+      case 3: f(IntC<3>{}); break;
+      case 4: f(IntC<4>{}); break;
+      case 5: f(IntC<5>{}); break;
+      case 6: f(IntC<6>{}); break;
+      case 7: f(IntC<7>{}); break;
+      default: f(IntC<0>{}); break;
+    }
+  }
+}
+
+// Geometry of one row pair against the target row's 16-byte grid: the target row's
+// first H entries (H < 16 / element bytes) lie before its first 16-byte boundary;
+// the body [H, V) is copied in whole 16-byte words.  The draft row's body starts
+// 2 * zs2 bytes past a 16-byte boundary (zs2 in 0..7).
+struct RowGeom {
+  int H;
+  int zs2;
+  const uint8_t* tb;  // target body (16-byte aligned)
+  const uint8_t* zb;  // draft body (may be off the grid), nullptr for a target-only row
+};
+
+template <class DZ, class DT>
+__device__ __forceinline__ RowGeom row_geom(const uint8_t* zrow, const uint8_t* trow, int V) {
+  RowGeom g;
+  const int off = static_cast<int>(reinterpret_cast<uintptr_t>(trow) & 15u);
+  g.H = min(((16 - off) & 15) / DT::kBytes, V);
+  g.tb = trow + static_cast<int64_t>(g.H) * DT::kBytes;
+  g.zb = zrow ? zrow + static_cast<int64_t>(g.H) * DZ::kBytes : nullptr;
+  g.zs2 = zrow ? static_cast<int>((reinterpret_cast<uintptr_t>(g.zb) & 15u) >> 1) : 0;
+  return g;
+}
+
+}  // namespace adaflash

@@ -129,13 +129,16 @@ struct LmCombineParams {
 void count_launch();
 
 // dtype codes match adaflash_dtype (0 = fp32, 1 = bf16)
-cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
-// The row pass with the gradient (single-pass forward + backward; rows on the
-// 16-byte grid).  Cluster size: rowpass_grad_cluster_size (row_bytes = V (b_z + b_t)).
+// The row pass (rows at any element-aligned address: each row follows its target
+// row's 16-byte grid).
+cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s);
+// The row pass with the gradient (single-pass forward + backward, any element-aligned
+// rows).  Cluster size: rowpass_grad_cluster_size (row_bytes = V (b_z + b_t)).
 cudaError_t launch_rowpass_grad(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s);
 int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int num_sms);
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
-cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s);
+// The backward (rows at any element-aligned address).
+cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, cudaStream_t s);
 // Fused forward + backward (K4).  fused_max_units is the largest batch (draft rows +
 // requests) the fused kernel is used for: 0 when a row pair does not fit a cluster's
 // shared memory; above it the caller runs K1 + K3, which stream faster on full waves.

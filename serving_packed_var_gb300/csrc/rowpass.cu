@@ -101,6 +101,16 @@ template <class DZ, class DT, bool kGrad>
 __host__ __device__ constexpr int chunk_of() {
   return DZ::kBytes + DT::kBytes <= 4 ? RowCfg<kGrad>::kChunk : RowCfg<kGrad>::kChunk / 2;
 }
+// One ring stage: the target chunk, then the draft chunk with 16 bytes of room for a
+// copy that starts at the 16-byte boundary below a draft body off the grid; the
+// stage rounded to 128 bytes.
+template <class DZ, class DT, bool kGrad>
+struct StageLayout {
+  static constexpr int kChunk = chunk_of<DZ, DT, kGrad>();
+  static constexpr int kZOff = kChunk * DT::kBytes;
+  static constexpr int kBytes = (kZOff + kChunk * DZ::kBytes + 16 + 127) / 128 * 128;
+};
+
 // With the gradient: L2 priority hints on the two passes' bulk copies (keep, then
 // drop), and the order of the second pass over a slice (1: last chunk first).
 #ifndef ADAFLASH_FB_L2_HINTS
@@ -124,7 +134,8 @@ struct RowGrad {
   float bg;      // beta * g, taken off at the target argmax
   float lse_z;
   float mt;      // the max of t
-  int ga;        // slice-local group holding the first max of t, -1 when not in this slice
+  int ga;        // slice-local body group holding the first max of t, -1 when not in this slice
+  int head_arg;  // the first max of t lies in the row's head, which this CTA holds
   int stop;      // a wait gave up: every consumer thread leaves together
 };
 
@@ -142,7 +153,15 @@ __device__ __forceinline__ float grad_of(float z, float t, const RowGrad& k) {
 // gradient, dz_v = g (p_v (m_v (r_v + 1) - S) + beta (p_v - [v == a])), written once
 // with streaming stores.  Every CTA of the cluster gets the corrections (every CTA
 // needs S).
-template <class DZ, class DT, bool kFast, bool kGrad>
+//
+// Rows need not start on the 16-byte grid.  A unit's vocabulary follows the target
+// row's grid: its first H entries (the head, before the target row's first 16-byte
+// boundary; H < 8) are group 0, read with element loads by rank 0, and the body
+// [H, V) is cut into 8-entry groups 1, 2, ... and into slices of the cluster.  The
+// target body is bulk-copied as it lies; the draft body, which may start 2 zs2
+// bytes past a boundary, is bulk-copied from the boundary below it (16 bytes more)
+// and read with aligned loads at that shift (one instance of the loop per shift).
+template <class DZ, class DT, bool kGrad>
 __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBlocks)
     rowpass_kernel(const RowPassParams P) {
   constexpr int kConsumerWarps = RowCfg<kGrad>::kWarps;
@@ -173,14 +192,15 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
 
   constexpr int kChunk = chunk_of<DZ, DT, kGrad>();
   constexpr int kGroupsPerThread = kChunk / 8 / kConsumers;  // 8-entry groups per consumer thread per chunk
-  constexpr int kStageZ = kChunk * DZ::kBytes;
   constexpr int kStageT = kChunk * DT::kBytes;
+  constexpr int kZOff = StageLayout<DZ, DT, kGrad>::kZOff;
+  constexpr int kStageBytes = StageLayout<DZ, DT, kGrad>::kBytes;
   // 128-byte aligned base for the bulk-copy ring (the launch adds 128 bytes of slack).
   uint8_t* ring =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
   // One screening code per consumer thread and slot: slot c < #chunks covers the
-  // thread's groups of ring chunk c, later slots one directly loaded group each.
-  uint16_t* codes = reinterpret_cast<uint16_t*>(ring + kStages * (kStageZ + kStageT));
+  // thread's groups of ring chunk c, the slot after them one directly loaded group.
+  uint16_t* codes = reinterpret_cast<uint16_t*>(ring + kStages * kStageBytes);
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -215,7 +235,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
 
   if (warp == kConsumerWarps) {
     // ---------------- producer warp: runs ahead across units ----------------
-    if (kFast && lane == 0) {
+    if (lane == 0) {
       uint32_t cc = 0;
       uint64_t keep = 0, drop = 0;
       if (kGrad) {
@@ -224,13 +244,15 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
       }
       for (int u = P.unit_begin + cid; u < num_units && !*abort_flag; u += ncl) {
         const Unit U = map_unit(P, u);
-        const int v_begin = static_cast<int>(rank) * P.slice;
-        const int v_end = U.bad ? v_begin : min(P.V, v_begin + P.slice);
-        const int body = max(0, v_end - v_begin) & ~7;
         const uint8_t* zrow =
             U.pair ? static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(U.d) * P.ld_z * DZ::kBytes : nullptr;
         const uint8_t* trow =
             static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(max(U.s, 0)) * P.ld_t * DT::kBytes;
+        const RowGeom G = row_geom<DZ, DT>(zrow, trow, P.V);
+        const int v_begin = static_cast<int>(rank) * P.slice;  // in the body
+        const int v_end = U.bad ? v_begin : min(P.V - G.H, v_begin + P.slice);
+        const int body = max(0, v_end - v_begin) & ~7;
+        const int zshift = 2 * G.zs2;  // bytes past the 16-byte boundary below the draft body
         const int passes = (kGrad && U.pair && !U.bad) ? 2 : 1;
         const int nch = (body + kChunk - 1) / kChunk;
         for (int pass = 0; pass < passes && !*abort_flag; ++pass) {
@@ -243,19 +265,19 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
               break;
             }
             const int n = min(kChunk, body - e0);
-            const uint32_t bz = U.pair ? static_cast<uint32_t>(n * DZ::kBytes) : 0u;
+            const uint32_t bz = U.pair ? static_cast<uint32_t>(n * DZ::kBytes + (zshift ? 16 : 0)) : 0u;
             const uint32_t bt = static_cast<uint32_t>(n * DT::kBytes);
             mbar_arrive_expect_tx(&full_bar[st], bz + bt);
-            uint8_t* stage = ring + st * (kStageZ + kStageT);
-            const uint8_t* zsrc = zrow + static_cast<int64_t>(v_begin + e0) * DZ::kBytes;
-            const uint8_t* tsrc = trow + static_cast<int64_t>(v_begin + e0) * DT::kBytes;
+            uint8_t* stage = ring + st * kStageBytes;
+            const uint8_t* zsrc = U.pair ? G.zb + static_cast<int64_t>(v_begin + e0) * DZ::kBytes - zshift : nullptr;
+            const uint8_t* tsrc = G.tb + static_cast<int64_t>(v_begin + e0) * DT::kBytes;
             if (kGrad && U.pair && kL2Hints) {
               const uint64_t pol = pass == 0 ? keep : drop;
-              bulk_copy_g2s_hint(stage, zsrc, bz, &full_bar[st], pol);
-              bulk_copy_g2s_hint(stage + kStageZ, tsrc, bt, &full_bar[st], pol);
+              bulk_copy_g2s_hint(stage + kZOff, zsrc, bz, &full_bar[st], pol);
+              bulk_copy_g2s_hint(stage, tsrc, bt, &full_bar[st], pol);
             } else {
-              if (U.pair) bulk_copy_g2s(stage, zsrc, bz, &full_bar[st]);
-              bulk_copy_g2s(stage + kStageZ, tsrc, bt, &full_bar[st]);
+              if (U.pair) bulk_copy_g2s(stage + kZOff, zsrc, bz, &full_bar[st]);
+              bulk_copy_g2s(stage, tsrc, bt, &full_bar[st]);
             }
           }
         }
@@ -274,19 +296,59 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
     int it = 0, pit = 0;
     for (int u = P.unit_begin + cid; u < num_units; u += ncl, ++it) {
       const Unit U = map_unit(P, u);
-      const int v_begin = static_cast<int>(rank) * P.slice;
-      const int v_end = U.bad ? v_begin : min(P.V, v_begin + P.slice);
-      const int len = max(0, v_end - v_begin);
-      const int ngroups = (len + 7) >> 3;
-      const int body = kFast ? (len & ~7) : 0;
       const uint8_t* zrow =
           U.pair ? static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(U.d) * P.ld_z * DZ::kBytes : nullptr;
       const uint8_t* trow =
           static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(max(U.s, 0)) * P.ld_t * DT::kBytes;
+      const RowGeom G = row_geom<DZ, DT>(zrow, trow, P.V);
+      const int Vb = P.V - G.H;
+      const int v_begin = static_cast<int>(rank) * P.slice;  // in the body
+      const int v_end = U.bad ? v_begin : min(Vb, v_begin + P.slice);
+      const int len = max(0, v_end - v_begin);
+      const int ngroups = (len + 7) >> 3;
+      // Direct group index ngroups stands for the head (rank 0 only).
+      const int has_head = (rank == 0 && !U.bad && G.H > 0) ? 1 : 0;
+      const int ngx = ngroups + has_head;
+      const int body = len & ~7;
+      const int gfirst = 1 + (v_begin >> 3);  // row-global index of the slice's first group
 
       Acc acc;
       acc_init(acc);
-      if (kFast) {
+      if (U.pair) {
+        // The draft body's shift picks the loop instance (uniform per unit).
+        dispatch_shift<DZ>(G.zs2, [&](auto zs_c) {
+          constexpr int ZS = decltype(zs_c)::value;
+          for (int e0 = 0; e0 < body; e0 += kChunk, ++cc) {
+            const int st = static_cast<int>(cc % kStages);
+            if (!mbar_wait_bounded(&full_bar[st], (cc / kStages) & 1)) {
+              atomicOr(&s_unit_err, 1);
+              *abort_flag = 1;
+              break;
+            }
+            const int gcount = min(kChunk, body - e0) >> 3;
+            const uint8_t* stage = ring + st * kStageBytes;
+            const uint32_t* zw = reinterpret_cast<const uint32_t*>(stage + kZOff);
+            const int gbase = gfirst + (e0 >> 3);
+            float cm = kNegInf;
+#pragma unroll
+            for (int k = 0; k < kGroupsPerThread; ++k) {
+              const int g = tid + k * kConsumers;
+              if (g < gcount) {
+                float z[8], t[8], vmt;
+                load8_shifted<DZ, ZS, false>(zw + g * 2 * DZ::kBytes, z);
+                const float vmz = max8(z);
+                load8_smem<DT>(stage, g, t, vmt);
+                acc_pair_nc(acc, z, t, vmz, vmt, gbase + g);
+                cm = fmaxf(cm, vmz);
+              }
+            }
+            acc.cmax = fmaxf(acc.cmax, cm);
+            codes[(e0 / kChunk) * kConsumers + tid] = code_up(cm);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[st]);
+          }
+        });
+      } else {
         for (int e0 = 0; e0 < body; e0 += kChunk, ++cc) {
           const int st = static_cast<int>(cc % kStages);
           if (!mbar_wait_bounded(&full_bar[st], (cc / kStages) & 1)) {
@@ -295,47 +357,31 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
             break;
           }
           const int gcount = min(kChunk, body - e0) >> 3;
-          const uint8_t* stage = ring + st * (kStageZ + kStageT);
-          const int gbase = (v_begin + e0) >> 3;  // row-global group index of the chunk's first group
-          if (U.pair) {
-            float cm = kNegInf;
+          const uint8_t* stage = ring + st * kStageBytes;
+          const int gbase = gfirst + (e0 >> 3);
 #pragma unroll
-            for (int k = 0; k < kGroupsPerThread; ++k) {
-              const int g = tid + k * kConsumers;
-              if (g < gcount) {
-                float z[8], t[8], vmz, vmt;
-                load8_smem<DZ>(stage, g, z, vmz);
-                load8_smem<DT>(stage + kStageZ, g, t, vmt);
-                acc_pair_nc(acc, z, t, vmz, vmt, gbase + g);
-                cm = fmaxf(cm, vmz);
-              }
-            }
-            acc.cmax = fmaxf(acc.cmax, cm);
-            codes[(e0 / kChunk) * kConsumers + tid] = code_up(cm);
-          } else {
-#pragma unroll
-            for (int k = 0; k < kGroupsPerThread; ++k) {
-              const int g = tid + k * kConsumers;
-              if (g < gcount) {
-                float t[8], vmt;
-                load8_smem<DT>(stage + kStageZ, g, t, vmt);
-                acc_target(acc, vmt, gbase + g);
-              }
+          for (int k = 0; k < kGroupsPerThread; ++k) {
+            const int g = tid + k * kConsumers;
+            if (g < gcount) {
+              float t[8], vmt;
+              load8_smem<DT>(stage, g, t, vmt);
+              acc_target(acc, vmt, gbase + g);
             }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty_bar[st]);
         }
       }
-      // Direct loads: the whole slice (unaligned rows) or the ragged tail group.
-      // Group g is always handled by consumer thread g mod 256 (in the ring loop as
-      // here), so a thread's group maximum covers exactly the groups it re-reads.
+      // Direct loads: the ragged end of the slice and (rank 0) the head.  Group g is
+      // always handled by consumer thread g mod kConsumers, so a thread's group maximum
+      // covers exactly the groups it re-reads.
       const int nchunks = (body + kChunk - 1) / kChunk;
       const int gd0 = (body >> 3) + ((tid - (body >> 3)) & (kConsumers - 1));  // this thread's first direct group
-      for (int g = gd0, slot = nchunks; g < ngroups; g += kConsumers, ++slot) {
-        const int64_t v0 = v_begin + (static_cast<int64_t>(g) << 3);
-        const int n = min(8, v_end - static_cast<int>(v0));
-        const int grp = static_cast<int>(v0 >> 3);
+      for (int g = gd0, slot = nchunks; g < ngx; g += kConsumers, ++slot) {
+        const bool head = g == ngroups;
+        const int v0 = head ? 0 : G.H + v_begin + (g << 3);
+        const int n = head ? G.H : min(8, v_end - (v_begin + (g << 3)));
+        const int grp = head ? 0 : gfirst + g;
         float t[8], vmt;
         load_global<DT>(trow, v0, n, t, vmt);
         if (U.pair) {
@@ -379,8 +425,9 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
         // holds that group (no re-read here).
         rc.bgrp = all.bgrp;
         rc.mt = all.mt;
-        rc.argmax = (rank == 0 && !U.bad && !(kGrad && U.pair)) ? resolve_argmax<DT>(trow, all.bgrp, all.mt, P.V)
-                                                                 : -1;
+        rc.argmax = (rank == 0 && !U.bad && !(kGrad && U.pair))
+                        ? resolve_argmax_grid<DT>(trow, all.bgrp, all.mt, P.V, G.H)
+                        : -1;
         rc.err = all.err | werr;
         rc.stop = *abort_flag;
         if (U.pair && !U.bad) {
@@ -433,7 +480,8 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
           P.row_stats[4 * d + 1] = rc.lse_t;
           P.row_stats[4 * d + 2] = (rc.kl_unclip + 1.f) - sclip_all;
           P.row_stats[4 * d + 3] = static_cast<float>(nclip_all);
-          if (err_all || rc.bgrp < 0 || rc.bgrp >= (P.V + 7) / 8) flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
+          if (err_all || rc.bgrp < (G.H > 0 ? 0 : 1) || rc.bgrp > (Vb + 7) / 8)
+            flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
         } else if (rc.argmax < 0 || rc.argmax >= P.V) {
           // only after an aborted unit (no group was reduced): nothing valid to write
           flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
@@ -463,8 +511,9 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
         k.bg = __fmul_rn(P.ce_weight, k.g);
         k.lse_z = rc.lse_z;
         k.mt = rc.mt;
-        const int ga = rc.bgrp - (v_begin >> 3);
-        k.ga = (ga >= 0 && ga < ngroups) ? ga : -1;
+        const int ga = rc.bgrp - gfirst;  // slice-local group of the first max of t
+        k.ga = (rc.bgrp >= 1 && ga >= 0 && ga < ngroups) ? ga : -1;
+        k.head_arg = (has_head && rc.bgrp == 0) ? 1 : 0;
         k.stop = *abort_flag;
         s_grad = k;
       };
@@ -490,24 +539,29 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
         if (!U.bad && rc.scan && acc.cmax > theta) {
           const TermConsts tc = make_term_consts(rc.lse_z, rc.lse_t);
           const float c = P.clip_c;
-          const int nchunks = (body + kChunk - 1) / kChunk;
-          const int gd0 = (body >> 3) + ((tid - (body >> 3)) & (kConsumers - 1));
-          const int nslots = nchunks + (ngroups > gd0 ? (ngroups - gd0 + kConsumers - 1) / kConsumers : 0);
+          const int nslots = nchunks + (ngx > gd0 ? (ngx - gd0 + kConsumers - 1) / kConsumers : 0);
           for (int slot = 0; slot < nslots; ++slot) {
             if (!(code_value(codes[slot * kConsumers + tid]) > theta)) continue;
             for (int k = 0; k < (slot < nchunks ? kGroupsPerThread : 1); ++k) {
-              int g;
+              int v0, n;
               if (slot < nchunks) {
                 const int gl = tid + k * kConsumers;
                 if (gl >= (min(kChunk, body - slot * kChunk) >> 3)) continue;
-                g = slot * (kChunk / 8) + gl;
+                const int g = slot * (kChunk / 8) + gl;
+                v0 = G.H + v_begin + (g << 3);
+                n = 8;
               } else {
-                g = gd0 + (slot - nchunks) * kConsumers;
+                const int g = gd0 + (slot - nchunks) * kConsumers;
+                if (g == ngroups) {
+                  v0 = 0;
+                  n = G.H;
+                } else {
+                  v0 = G.H + v_begin + (g << 3);
+                  n = min(8, v_end - (v_begin + (g << 3)));
+                }
               }
-              const int v0 = v_begin + (g << 3);
-              const int n = min(8, v_end - v0);
               float zs[8], ts[8];
-              if (kFast && n == 8) {
+              if (n == 8 && G.zs2 == 0 && v0 >= G.H) {
                 load8_global_vec<DZ>(zrow, v0, zs);
                 load8_global_vec<DT>(trow, v0, ts);
               } else {
@@ -581,77 +635,86 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
         if (!U.bad) {
           // ---- second pass over the slice (from L2): dz, written once ----
           const RowGrad k = s_grad;
-          float* grow = P.grad + static_cast<int64_t>(U.d) * P.ld_g + v_begin;
+          float* grow = P.grad + static_cast<int64_t>(U.d) * P.ld_g;  // the row
+          float* gbody = grow + G.H + v_begin;                          // this slice of the body
+          const int gq = static_cast<int>((reinterpret_cast<uintptr_t>(gbody) >> 2) & 3u);
           const int nch = (body + kChunk - 1) / kChunk;
-          for (int ci = 0; ci < nch; ++ci, ++cc) {
-            const int e0 = kReverseP2 ? (nch - 1 - ci) * kChunk : ci * kChunk;
-            const int st = static_cast<int>(cc % kStages);
-            if (!mbar_wait_bounded(&full_bar[st], (cc / kStages) & 1)) {
-              atomicOr(&s_unit_err, 1);
-              *abort_flag = 1;
-              break;
-            }
-            const int gcount = min(kChunk, body - e0) >> 3;
-            const uint8_t* stage = ring + st * (kStageZ + kStageT);
-#pragma unroll
-            for (int kk = 0; kk < kGroupsPerThread; ++kk) {
-              const int g = tid + kk * kConsumers;
-              if (g < gcount) {
-                float z[8], t[8], out[8], vm;
-                load8_smem<DZ>(stage, g, z, vm);
-                load8_smem<DT>(stage + kStageZ, g, t, vm);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) out[e] = grad_of(z[e], t[e], k);
-                float4* dst = reinterpret_cast<float4*>(grow + e0 + (g << 3));
-                __stcs(dst, make_float4(out[0], out[1], out[2], out[3]));
-                __stcs(dst + 1, make_float4(out[4], out[5], out[6], out[7]));
+          dispatch_shift<DZ>(G.zs2, [&](auto zs_c) {
+            constexpr int ZS = decltype(zs_c)::value;
+            for (int ci = 0; ci < nch; ++ci, ++cc) {
+              const int e0 = kReverseP2 ? (nch - 1 - ci) * kChunk : ci * kChunk;
+              const int st = static_cast<int>(cc % kStages);
+              if (!mbar_wait_bounded(&full_bar[st], (cc / kStages) & 1)) {
+                atomicOr(&s_unit_err, 1);
+                *abort_flag = 1;
+                break;
               }
-            }
-            // The group holding the first max of t: the thread that just wrote it finds
-            // the index, rewrites that entry with the hard-label term (program order makes
-            // it the final value) and writes the argmax and the cross-entropy.
-            const int lc = k.ga - (e0 >> 3);
-            if (lc >= 0 && lc < gcount && tid == (lc & (kConsumers - 1))) {
-              float zz[8], tt[8], vm;
-              load8_smem<DZ>(stage, lc, zz, vm);
-              load8_smem<DT>(stage + kStageZ, lc, tt, vm);
-              int j = -1;
-              float zj = 0.f, tj = 0.f;
+              const int gcount = min(kChunk, body - e0) >> 3;
+              const uint8_t* stage = ring + st * kStageBytes;
+              const uint32_t* zw = reinterpret_cast<const uint32_t*>(stage + kZOff);
 #pragma unroll
-              for (int e = 7; e >= 0; --e)
-                if (tt[e] == k.mt) {
-                  j = e;
-                  zj = zz[e];
-                  tj = tt[e];
+              for (int kk = 0; kk < kGroupsPerThread; ++kk) {
+                const int g = tid + kk * kConsumers;
+                if (g < gcount) {
+                  float z[8], t[8], out[8], vm;
+                  load8_shifted<DZ, ZS, false>(zw + g * 2 * DZ::kBytes, z);
+                  load8_smem<DT>(stage, g, t, vm);
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) out[e] = grad_of(z[e], t[e], k);
+                  store8_stream(gbody + e0 + (g << 3), gq, out);
                 }
-              if (j >= 0) {
-                const int la = e0 + (lc << 3) + j;
-                grow[la] = __fsub_rn(grad_of(zj, tj, k), k.bg);
-                P.target_argmax[U.s] = v_begin + la;
-                P.ce_row[U.d] = k.lse_z - zj;
-              } else {
-                flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
               }
+              // The group holding the first max of t: the thread that just wrote it finds
+              // the index, rewrites that entry with the hard-label term (program order makes
+              // it the final value) and writes the argmax and the cross-entropy.
+              const int lc = k.ga - (e0 >> 3);
+              if (lc >= 0 && lc < gcount && tid == (lc & (kConsumers - 1))) {
+                float zz[8], tt[8], vm;
+                load8_shifted<DZ, ZS, false>(zw + lc * 2 * DZ::kBytes, zz);
+                load8_smem<DT>(stage, lc, tt, vm);
+                int j = -1;
+                float zj = 0.f, tj = 0.f;
+#pragma unroll
+                for (int e = 7; e >= 0; --e)
+                  if (tt[e] == k.mt) {
+                    j = e;
+                    zj = zz[e];
+                    tj = tt[e];
+                  }
+                if (j >= 0) {
+                  const int la = e0 + (lc << 3) + j;
+                  gbody[la] = __fsub_rn(grad_of(zj, tj, k), k.bg);
+                  P.target_argmax[U.s] = G.H + v_begin + la;
+                  P.ce_row[U.d] = k.lse_z - zj;
+                } else {
+                  flag_status(P.status, ADAFLASH_ERR_TIMEOUT);
+                }
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&empty_bar[st]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[st]);
-          }
-          // the ragged end of the slice (fewer than 8 entries) straight from global memory;
-          // each entry is written by one thread, the argmax by the thread holding it
-          for (int v = body + tid; v < len; v += kConsumers) {
-            const float zv = DZ::load(zrow, v_begin + v), tv = DT::load(trow, v_begin + v);
+          });
+          // The ragged end of the slice (fewer than 8 entries) and, in rank 0, the head,
+          // straight from global memory; each entry is written by one thread, the argmax
+          // by the thread holding it (the first entry of its group equal to the max).
+          auto direct_entry = [&](int v, int g0, bool arg_group) {
+            const float zv = DZ::load(zrow, v), tv = DT::load(trow, v);
             float o = grad_of(zv, tv, k);
-            if (k.ga == (body >> 3) && tv == k.mt) {
+            if (arg_group && tv == k.mt) {
               bool first = true;
-              for (int u = body; u < v; ++u) first = first && !(DT::load(trow, v_begin + u) == k.mt);
+              for (int u2 = g0; u2 < v; ++u2) first = first && !(DT::load(trow, u2) == k.mt);
               if (first) {
                 o = __fsub_rn(o, k.bg);
-                P.target_argmax[U.s] = v_begin + v;
+                P.target_argmax[U.s] = v;
                 P.ce_row[U.d] = k.lse_z - zv;
               }
             }
             grow[v] = o;
-          }
+          };
+          for (int v = body + tid; v < len; v += kConsumers)
+            direct_entry(G.H + v_begin + v, G.H + v_begin + body, k.ga == (body >> 3));
+          if (has_head)
+            for (int v = tid; v < G.H; v += kConsumers) direct_entry(v, 0, k.head_arg != 0);
         }
       } else {
         if (stop) break;
@@ -723,22 +786,21 @@ static int sm_count() {
   return n;
 }
 
-template <class DZ, class DT, bool kFast, bool kGrad>
+template <class DZ, class DT, bool kGrad>
 static size_t rowpass_smem(int slice) {
   constexpr int kChunk = chunk_of<DZ, DT, kGrad>();
   constexpr int kConsumers = RowCfg<kGrad>::kConsumers;
-  const size_t ring = static_cast<size_t>(kStages) * kChunk * (DZ::kBytes + DT::kBytes);
-  // screening codes: per consumer thread one slot per ring chunk (+1 for a ragged
-  // tail group) on the bulk-copy path, one per group on the direct-load path
-  const int groups = (slice + 7) / 8;
-  const int slots = kFast ? ((slice + kChunk - 1) / kChunk + 1) : ((groups + kConsumers - 1) / kConsumers);
+  const size_t ring = static_cast<size_t>(kStages) * StageLayout<DZ, DT, kGrad>::kBytes;
+  // screening codes: per consumer thread one slot per ring chunk, +1 for its one
+  // directly loaded group (the ragged end of the slice or the head)
+  const int slots = (slice + kChunk - 1) / kChunk + 1;
   return 128 + ring + static_cast<size_t>(slots) * kConsumers * sizeof(uint16_t);
 }
 
 // Co-resident clusters of this kernel at this cluster size (cached).
-template <class DZ, class DT, bool kFast, bool kGrad>
+template <class DZ, class DT, bool kGrad>
 static int active_clusters(int cluster, size_t smem) {
-  auto kern = rowpass_kernel<DZ, DT, kFast, kGrad>;
+  auto kern = rowpass_kernel<DZ, DT, kGrad>;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return 1;
   // The query must see the shared-memory size the launch will use.
@@ -772,15 +834,15 @@ static int active_clusters(int cluster, size_t smem) {
 }
 
 // One launch over units [p.unit_begin, p.unit_end), persistent clusters.
-template <class DZ, class DT, bool kFast, bool kGrad>
+template <class DZ, class DT, bool kGrad>
 static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaStream_t stream) {
-  const size_t smem = rowpass_smem<DZ, DT, kFast, kGrad>(p.slice);
-  auto kern = rowpass_kernel<DZ, DT, kFast, kGrad>;
+  const size_t smem = rowpass_smem<DZ, DT, kGrad>(p.slice);
+  auto kern = rowpass_kernel<DZ, DT, kGrad>;
   const int units = p.unit_end - p.unit_begin;
   if (units <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int clusters = active_clusters<DZ, DT, kFast, kGrad>(p.cluster, smem);
+  const int clusters = active_clusters<DZ, DT, kGrad>(p.cluster, smem);
   cudaLaunchConfig_t cfg = {};
   const int grid_clusters = units < clusters ? units : clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters) * static_cast<unsigned>(p.cluster), 1, 1);
@@ -808,7 +870,7 @@ static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaS
 // Every launch is programmatic: the first one waits for the stream's previous
 // kernel before touching global memory; a second one starts as CTAs of the first
 // retire and completes only after the first.
-template <class DZ, class DT, bool kFast, bool kGrad = false>
+template <class DZ, class DT, bool kGrad = false>
 static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   const int units = (p0.mode == kModeVerify) ? p0.N_t : (p0.N_d + p0.R);
   if (units <= 0) return cudaSuccess;
@@ -816,16 +878,16 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   p.unit_begin = 0;
   p.unit_end = units;
   p.wait_prior = 0;
-  const int clusters = active_clusters<DZ, DT, kFast, kGrad>(p.cluster, rowpass_smem<DZ, DT, kFast, kGrad>(p.slice));
+  const int clusters = active_clusters<DZ, DT, kGrad>(p.cluster, rowpass_smem<DZ, DT, kGrad>(p.slice));
   const int split = (units / clusters) * clusters;
   // With the gradient, a last partial wave of target-only rows (cheap: no second pass)
   // stays in the one launch rather than costing a launch of its own.
   if (!ADAFLASH_ROWPASS_TAIL || units <= clusters || split == units || p.cluster >= kMaxCluster ||
       (kGrad && p0.mode == kModeFwd && split >= p0.N_d))
-    return launch_range<DZ, DT, kFast, kGrad>(p, true, stream);
+    return launch_range<DZ, DT, kGrad>(p, true, stream);
   const RowPassParams base = p;
   p.unit_end = split;
-  cudaError_t e = launch_range<DZ, DT, kFast, kGrad>(p, true, stream);
+  cudaError_t e = launch_range<DZ, DT, kGrad>(p, true, stream);
   if (e != cudaSuccess) return e;
   auto launch_tail = [&](int b, int end) {
     RowPassParams tail = base;
@@ -843,7 +905,7 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
     }
     if (tail.cluster < p.cluster) tail.cluster = p.cluster;
     tail.slice = rowpass_slice(p.V, tail.cluster);
-    return launch_range<DZ, DT, kFast, kGrad>(tail, true, stream);
+    return launch_range<DZ, DT, kGrad>(tail, true, stream);
   };
   // With the gradient, leftover paired rows and the cheap target-only rows get their
   // own launches, so the few expensive rows are split over the larger clusters their
@@ -873,24 +935,18 @@ int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int num_sms) 
 
 cudaError_t launch_rowpass_grad(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s) {
   const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
-  if (zb && tb) return launch_one<BF16, BF16, true, true>(p, s);
-  if (!zb && tb) return launch_one<F32, BF16, true, true>(p, s);
-  if (zb && !tb) return launch_one<BF16, F32, true, true>(p, s);
-  return launch_one<F32, F32, true, true>(p, s);
+  if (zb && tb) return launch_one<BF16, BF16, true>(p, s);
+  if (!zb && tb) return launch_one<F32, BF16, true>(p, s);
+  if (zb && !tb) return launch_one<BF16, F32, true>(p, s);
+  return launch_one<F32, F32, true>(p, s);
 }
 
-cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool fast, cudaStream_t s) {
+cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s) {
   const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
-  if (fast) {
-    if (zb && tb) return launch_one<BF16, BF16, true>(p, s);
-    if (!zb && tb) return launch_one<F32, BF16, true>(p, s);
-    if (zb && !tb) return launch_one<BF16, F32, true>(p, s);
-    return launch_one<F32, F32, true>(p, s);
-  }
-  if (zb && tb) return launch_one<BF16, BF16, false>(p, s);
-  if (!zb && tb) return launch_one<F32, BF16, false>(p, s);
-  if (zb && !tb) return launch_one<BF16, F32, false>(p, s);
-  return launch_one<F32, F32, false>(p, s);
+  if (zb && tb) return launch_one<BF16, BF16>(p, s);
+  if (!zb && tb) return launch_one<F32, BF16>(p, s);
+  if (zb && !tb) return launch_one<BF16, F32>(p, s);
+  return launch_one<F32, F32>(p, s);
 }
 
 }  // namespace adaflash

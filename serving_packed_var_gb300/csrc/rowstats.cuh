@@ -366,3 +366,30 @@ __device__ __forceinline__ Unit map_unit(const RowPassParams& P, int u) {
 }  // namespace
 
 }  // namespace adaflash
+
+namespace adaflash {
+namespace {
+
+// Lowest index of the value mt inside row-global group grp of a target row whose
+// groups follow its 16-byte grid: group 0 is the head [0, H) and group G >= 1 holds
+// entries [H + 8 (G - 1), H + 8 G) (-1 if absent or out of range).
+template <class DT>
+__device__ int resolve_argmax_grid(const uint8_t* trow, int grp, float mt, int V, int H) {
+  if (grp < 0) return -1;
+  int v0, n;
+  if (grp == 0) {
+    v0 = 0;
+    n = H;
+  } else {
+    const long long s = static_cast<long long>(H) + 8ll * (grp - 1);
+    if (s >= V) return -1;
+    v0 = static_cast<int>(s);
+    n = min(8, V - v0);
+  }
+  for (int j = 0; j < n; ++j)
+    if (DT::load(trow, v0 + j) == mt) return v0 + j;
+  return -1;
+}
+
+}  // namespace
+}  // namespace adaflash

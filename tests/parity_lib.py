@@ -49,13 +49,18 @@ def to_device(arr: np.ndarray, dtype: str, dev, misalign: int = 0) -> torch.Tens
 
 
 class GpuRun:
-    def __init__(self, batch, dev="cuda:0", bwd=True, grad_row=None, grad_scale=1.0, misalign=0, canary=16):
+    """The forward, then (bwd) the backward, as separate calls.  misalign shifts the base
+    pointers of both logit tensors by that many elements; misalign_z / misalign_t set
+    them apart and misalign_g shifts the gradient's base."""
+
+    def __init__(self, batch, dev="cuda:0", bwd=True, grad_row=None, grad_scale=1.0, misalign=0, canary=16,
+                 misalign_z=None, misalign_t=None, misalign_g=0):
         w = batch.w
         self.b = batch
         self.w = w
         dev = torch.device(dev)
-        self.z = to_device(batch.draft, w.d_dtype, dev, misalign)
-        self.t = to_device(batch.target, w.t_dtype, dev, misalign)
+        self.z = to_device(batch.draft, w.d_dtype, dev, misalign if misalign_z is None else misalign_z)
+        self.t = to_device(batch.target, w.t_dtype, dev, misalign if misalign_t is None else misalign_t)
         self.tok = torch.from_numpy(batch.tokens).to(dev)
         self.doff = torch.from_numpy(batch.doff).to(dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -86,9 +91,11 @@ class GpuRun:
         if bwd:
             self.grad_row = None if grad_row is None else torch.from_numpy(
                 np.asarray(grad_row, dtype=np.float32)).to(dev)
-            gfull = torch.full((Nd * w.vocab + canary,), -7.0, dtype=torch.float32, device=dev)
-            self._bufs["grad"] = (gfull, Nd * w.vocab, -7.0)
-            g = gfull[:Nd * w.vocab].view(Nd, w.vocab)
+            mg = misalign_g
+            gfull = torch.full((mg + Nd * w.vocab + canary,), -7.0, dtype=torch.float32, device=dev)
+            self._bufs["grad"] = (gfull, mg + Nd * w.vocab, -7.0)
+            self._heads = [(gfull, mg, -7.0)]
+            g = gfull[mg:mg + Nd * w.vocab].view(Nd, w.vocab)
             self.grad = af.adaflash_opd_loss_bwd(self.z, self.t, self.doff, self.out["target_argmax"],
                                                  self.out["row_stats"], w.clip_c, w.ce_weight,
                                                  grad_row=self.grad_row, grad_scale=grad_scale, vocab=w.vocab,
@@ -102,6 +109,9 @@ class GpuRun:
             tail = full[n:].cpu()
             if not bool((tail == fill).all()):
                 return name
+        for full, n, fill in getattr(self, "_heads", []):
+            if n and not bool((full[:n].cpu() == fill).all()):
+                return "grad head"
         return None
 
     def grad_rows(self, rows):

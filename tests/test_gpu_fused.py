@@ -33,12 +33,13 @@ def _lib():
 
 
 class FusedRun:
-    def __init__(self, b, grad_row=None, grad_scale=1.0, misalign=0, canary=16, ld_g=None):
+    def __init__(self, b, grad_row=None, grad_scale=1.0, misalign=0, canary=16, ld_g=None, misalign_z=None,
+                 misalign_t=None, misalign_g=0):
         import serving_packed_var_gb300 as af
         w = b.w
         dev = torch.device("cuda:0")
-        z = to_device(b.draft, w.d_dtype, dev, misalign)
-        t = to_device(b.target, w.t_dtype, dev, misalign)
+        z = to_device(b.draft, w.d_dtype, dev, misalign if misalign_z is None else misalign_z)
+        t = to_device(b.target, w.t_dtype, dev, misalign if misalign_t is None else misalign_t)
         tok = torch.from_numpy(b.tokens).to(dev)
         doff = torch.from_numpy(b.doff).to(dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -52,8 +53,10 @@ class FusedRun:
             return full[:n]
 
         ldg = w.vocab if ld_g is None else ld_g
-        gfull = torch.full((Nd * ldg + canary,), -7.0, dtype=torch.float32, device=dev)
-        self._bufs["grad"] = (gfull, Nd * ldg, -7.0)
+        mg = misalign_g
+        gfull = torch.full((mg + Nd * ldg + canary,), -7.0, dtype=torch.float32, device=dev)
+        self._bufs["grad"] = (gfull, mg + Nd * ldg, -7.0)
+        self._head = (gfull, mg, -7.0)
         out = dict(target_argmax=buf("target_argmax", Nt, torch.int32, -7),
                    accept_len=buf("accept_len", R, torch.int32, -7),
                    bonus_token=buf("bonus_token", R, torch.int32, -7),
@@ -62,7 +65,7 @@ class FusedRun:
                    ce_row=buf("ce_row", Nd, torch.float32, -7.0),
                    loss=buf("loss", 1, torch.float32, -7.0),
                    row_stats=buf("row_stats", 4 * Nd, torch.float32, -7.0).view(Nd, 4),
-                   grad=gfull[:Nd * ldg].view(Nd, ldg)[:, :w.vocab])
+                   grad=gfull[mg:mg + Nd * ldg].view(Nd, ldg)[:, :w.vocab])
         gr = None if grad_row is None else torch.from_numpy(np.asarray(grad_row, dtype=np.float32)).to(dev)
         self.out = af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_row=gr,
                                                 grad_scale=grad_scale, vocab=w.vocab, out=out, status=self.status)
@@ -79,12 +82,15 @@ class FusedRun:
         for name, (full, n, fill) in self._bufs.items():
             if not bool((full[n:].cpu() == fill).all()):
                 return name
+        full, n, fill = self._head
+        if n and not bool((full[:n].cpu() == fill).all()):
+            return "grad head"
         return None
 
 
-def _close_to_separate(b, grad_row=None, grad_scale=1.0, misalign=0, oracle_grad_rows=None):
-    f = FusedRun(b, grad_row=grad_row, grad_scale=grad_scale, misalign=misalign)
-    s = GpuRun(b, bwd=True, grad_row=grad_row, grad_scale=grad_scale, misalign=misalign)
+def _close_to_separate(b, grad_row=None, grad_scale=1.0, misalign=0, oracle_grad_rows=None, **shifts):
+    f = FusedRun(b, grad_row=grad_row, grad_scale=grad_scale, misalign=misalign, **shifts)
+    s = GpuRun(b, bwd=True, grad_row=grad_row, grad_scale=grad_scale, misalign=misalign, **shifts)
     assert f.status_word == s.status_word == 0, (f.status_word, s.status_word)
     assert f.canaries_intact() is None, f.canaries_intact()
     for k in INT_KEYS:
@@ -185,7 +191,7 @@ def test_streaming_ragged_vocab_padded_rows():
 
 
 @pytest.mark.parametrize("misalign", [1, 3])
-def test_unaligned_rows_take_the_separate_path(misalign):
+def test_unaligned_rows_take_the_row_pass_with_the_gradient(misalign):
     _close_to_separate(materialize(custom(vocab=5000, k=[3, 8])), misalign=misalign)
 
 
