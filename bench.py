@@ -182,10 +182,26 @@ def barrier():
 # our arm
 # ---------------------------------------------------------------------------
 
+K_MIX = {
+    "tiny": "k_i = {16, 9, 3, 1}, L_i ~ U{0..k_i}",
+    "single": "k = 16, L ~ U{0..16}",
+    "c32": "k_i ~ U{1..16}, L_i ~ Bin(k_i, 0.6)",
+    "c128": "k_i truncated-geometric (p = 0.07) on 1..16, L_i ~ Bin(k_i, 0.6), 5% of rows with 64 entries at "
+            "target -30 / draft +6",
+    "c128_clip": "as c128 with draft +16 on the planted entries",
+    "stress": "k_i = 16, L_i ~ U{0..16}, 1% exact-tie target rows, 1% draft == target rows, rows off the "
+              "16-byte grid (ld = V)",
+}
+
+
+def workload_text(w):
+    return (f"{w.name}: concurrency {w.num_requests}, V={w.vocab}, {w.d_dtype} draft / {w.t_dtype} target, "
+            f"{K_MIX.get(w.name, 'k_i as generated')}, clip c={w.clip_c}")
+
+
 def workload_config(w):
     return {
-        "workload": f"{w.name}: concurrency {w.num_requests}, V={w.vocab}, {w.d_dtype} draft / {w.t_dtype} target, "
-                    f"k_i truncated-geometric on 1..16, clip c={w.clip_c}, fwd+bwd",
+        "workload": workload_text(w) + ", fwd+bwd",
         "num_requests": w.num_requests, "draft_rows": w.num_draft_rows, "target_rows": w.num_target_rows,
         "vocab": w.vocab, "input_dtype": w.d_dtype, "clip_c": w.clip_c, "ce_weight": w.ce_weight,
         "l2": "inputs larger than L2 (no flush): forward reads and backward traffic exceed 129 MB",
@@ -371,12 +387,16 @@ def run_ours(args):
     # concurrency 1 (one request of 16 draft rows): the step eager and replayed from a CUDA graph
     small = run_small_batch_graph(dev, af, torch, np, make_workload, materialize)
 
+    # the other benchmark configurations (concurrency 1 and 32, the stress batch)
+    configs = run_configs(dev, af, torch, np, stream, hbm_peak()[0], make_workload, materialize)
+
     # the logit-free forward from hidden states at Qwen3-8B shapes (H = 4096, shared head),
     # the same packed layout as this workload
     lm = run_lmhead(args, w, dev, af, torch, np, stream)
 
     # end to end: pinned host inputs -> device, step, verify outputs + loss back to host
     e2e = run_e2e(args, b, w, dev, af, torch, np)
+    e2e_grad = run_e2e(args, b, w, dev, af, torch, np, grad_to_host=True)
 
     if rank != 0:
         if world > 1:
@@ -439,7 +459,7 @@ def run_ours(args):
                                             "L2 combine + K2 (adaflash_lmhead_opd_fwd), calls back to back",
                                  "ms": lm["ms"], "flops": lm["flops"], "achieved_tflops": lm["tflops"],
                                  "frac": lm["tflops"] / tpeak, "rows_per_s": Nd / (lm["ms"] * 1e-3),
-                                 "hidden": lm["hidden"], "vocab": lm["vocab"]}
+                                 "hidden": lm["hidden"], "vocab": lm["vocab"], "e2e": lm["e2e"]}
         roofline_lmhead = {"bound": "tensor", "achieved": lm["tflops"], "peak": tpeak, "unit": "TFLOP/s",
                            "frac": lm["tflops"] / tpeak,
                            "traffic": traffic.get("lmhead_gemm_kernel", {}).get("dram_bytes_per_launch"),
@@ -452,13 +472,19 @@ def run_ours(args):
                     "kernel": "fused verify + loss forward (K1 + K2), calls back to back",
                     "algorithmic_bytes_per_launch": fb, "in_step_frac": fwd_gbs / peak}
     value = whole_job_rows_per_s(Nd, world, ms, K)
+    head_cfg = {"workload": workload_text(w), "draft_rows": Nd, "target_rows": w.num_target_rows,
+                "fwd": _entry(fwd_alone_ms, fb, Nd, peak), "step": _entry(fwd_bwd_ms, spb, Nd, peak),
+                "note": "the headline configuration: the step is the timed region above"}
+    order = ["single", "c32", w.name, "stress"]
+    all_configs = {k: (head_cfg if k == w.name else configs[k]) for k in dict.fromkeys(order) if
+                   k == w.name or k in configs}
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded; no datasets or weights)",
         "config": workload_config(w), "roofline": roofline, "roofline_fwd": roofline_fwd, "roofline_bwd": roofline_bwd,
-        "roofline_lmhead": roofline_lmhead, "kernels": kernels, "small_batch": small, "cold": cold,
-        "e2e": e2e, "gpu_launches": launches, "clocks": clk.summary(),
+        "roofline_lmhead": roofline_lmhead, "kernels": kernels, "configs": all_configs, "small_batch": small, "cold": cold,
+        "e2e": e2e, "e2e_grad_to_host": e2e_grad, "gpu_launches": launches, "clocks": clk.summary(),
         "cpu_baseline": cpu_baseline(b) if world == 1 or rank == 0 else None,
         "impl": "ours",
     }
@@ -517,6 +543,114 @@ def run_cold(w, dev, af, torch, np, z, t, tok, doff, status, out, grad, stream, 
             "step_us": {"median": q(stp, 0.5), "p10": q(stp, 0.1), "p90": q(stp, 0.9)},
             "fwd_us": {"median": q(fwd, 0.5), "p10": q(fwd, 0.1), "p90": q(fwd, 0.9)},
             "bwd_us": {"median": q(bwd, 0.5), "p10": q(bwd, 0.1), "p90": q(bwd, 0.9)}}
+
+
+def _entry(ms, nbytes, rows, peak):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": ms, "bytes": nbytes, "achieved_gbs": gbs, "frac": gbs / peak, "rows_per_s": rows / (ms * 1e-3)}
+
+
+def _back_to_back(torch, stream, fn, n, warm_s=0.3):
+    """Mean time per call (ms) of n calls back to back on `stream`, after about warm_s of warm-up calls."""
+    t0, k = time.perf_counter(), 0
+    while k < 3 or (time.perf_counter() - t0 < warm_s and k < 5000):
+        fn()
+        k += 1
+        if k % 8 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def _graph_replay(torch, fn, n):
+    """Mean time per replay (ms) of fn captured once in a CUDA graph."""
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    for _ in range(20):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def run_configs(dev, af, torch, np, stream, peak, make_workload, materialize):
+    """Every benchmark configuration besides the headline one, each on its own batch:
+    concurrency 1 (the forward alone, as the configuration states, eager and replayed from
+    a CUDA graph; and the single-call step), concurrency 32 (the step and the forward) and
+    the stress batch (the step, the forward, the separate calls and greedy verification).
+    Times are means over calls back to back; bytes are algorithmic (every logit byte read
+    once, dz written once)."""
+    res = {}
+    for name in ("single", "c32", "stress"):
+        b = materialize(make_workload(name))
+        w = b.w
+        Nd, R, V = w.num_draft_rows, w.num_requests, w.vocab
+
+        def dev_from(arr, dtype):
+            if dtype == "bf16":
+                return torch.from_numpy(arr.view(np.int16)).to(dev).view(torch.bfloat16)
+            return torch.from_numpy(arr).to(dev)
+
+        z, t = dev_from(b.draft, w.d_dtype), dev_from(b.target, w.t_dtype)
+        tok, doff = torch.from_numpy(b.tokens).to(dev), torch.from_numpy(b.doff).to(dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        grad = torch.empty((Nd, V), dtype=torch.float32, device=dev)
+        fb, bb = algorithmic_bytes(w)
+        spb = single_pass_bytes(w)
+        o = {"out": af.adaflash_opd_loss_fwd(z, t, tok, doff, w.clip_c, w.ce_weight, status=st)}
+        fbo = af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_scale=1.0 / Nd,
+                                           out={"grad": grad}, status=st)
+
+        def fwd():
+            af.adaflash_opd_loss_fwd(z, t, tok, doff, w.clip_c, w.ce_weight, out=o["out"], status=st)
+
+        def step():
+            af.adaflash_opd_loss_fwd_bwd(z, t, tok, doff, w.clip_c, w.ce_weight, grad_scale=1.0 / Nd, out=fbo,
+                                         status=st)
+
+        n = {"single": 400, "c32": 200, "stress": 40}[name]
+        e = {"workload": workload_text(w), "draft_rows": Nd, "target_rows": w.num_target_rows}
+        e["fwd"] = _entry(_back_to_back(torch, stream, fwd, n), fb, Nd, peak)
+        e["step"] = _entry(_back_to_back(torch, stream, step, n), spb, Nd, peak)
+        if name == "single":
+            e["fwd_graph"] = _entry(_graph_replay(torch, fwd, n), fb, Nd, peak)
+            e["step_graph"] = _entry(_graph_replay(torch, step, n), spb, Nd, peak)
+        if name == "stress":
+            def separate():
+                fwd()
+                af.adaflash_opd_loss_bwd(z, t, doff, o["out"]["target_argmax"], o["out"]["row_stats"], w.clip_c,
+                                         w.ce_weight, grad_scale=1.0 / Nd, out=grad, status=st)
+            e["step_separate"] = _entry(_back_to_back(torch, stream, separate, n), fb + bb, Nd, peak)
+            vo = {"v": af.adaflash_verify_packed(t, tok, doff, status=st)}
+
+            def verify():
+                af.adaflash_verify_packed(t, tok, doff, out=vo["v"], status=st)
+            e["verify_packed"] = _entry(_back_to_back(torch, stream, verify, n),
+                                        w.num_target_rows * w.bytes_per_target_elem * V, Nd, peak)
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())} ({name})")
+        res[name] = e
+        del z, t, grad, o, fbo
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_small_batch_graph(dev, af, torch, np, make_workload, materialize):
@@ -599,14 +733,55 @@ def run_lmhead(args, w, dev, af, torch, np, stream):
         raise RuntimeError(f"device status {int(st.item())} (lmhead)")
     ms = a.elapsed_time(b) / n
     flops = 2.0 * (2 * Nd + R) * lw.hidden * lw.vocab
-    del hd, ht, wh, ws
-    return {"ms": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12, "hidden": lw.hidden, "vocab": lw.vocab}
+
+    # End to end: every step copies the draft and target hidden states (and the tokens and
+    # offsets) from pinned host memory, runs the call with the head resident on the device,
+    # and reads the verification outputs and the loss back.
+    hdh = torch.from_numpy(np.ascontiguousarray(lb.hd).view(np.int16)).pin_memory()
+    hth = torch.from_numpy(np.ascontiguousarray(lb.ht).view(np.int16)).pin_memory()
+    tokh, doffh = torch.from_numpy(lb.tokens).pin_memory(), torch.from_numpy(lb.doff).pin_memory()
+    hdd, htd = torch.empty_like(hdh, device=dev), torch.empty_like(hth, device=dev)
+    tokd, doffd = torch.empty_like(tokh, device=dev), torch.empty_like(doffh, device=dev)
+    res_h = {k: torch.empty(R, dtype=dt).pin_memory() for k, dt in
+             (("accept_len", torch.int32), ("bonus_token", torch.int32), ("accept_rate", torch.float32))}
+    res_h["loss"] = torch.empty(1, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        hdd.copy_(hdh, non_blocking=True)
+        htd.copy_(hth, non_blocking=True)
+        tokd.copy_(tokh, non_blocking=True)
+        doffd.copy_(doffh, non_blocking=True)
+        af.adaflash_lmhead_opd_fwd(hdd.view(torch.bfloat16), htd.view(torch.bfloat16), wh, wh, tokd, doffd,
+                                   lw.clip_c, lw.ce_weight, workspace=ws, out=out, status=st)
+        for k2, v in res_h.items():
+            v.copy_(out[k2], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        e2e_step()
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    bi = sum(x.numel() * x.element_size() for x in (hdh, hth, tokh, doffh))
+    bo = sum(x.numel() * x.element_size() for x in res_h.values())
+    e2e = {"value": Nd * n / el, "unit": "rows/s", "ms_per_step": el / n * 1e3, "h2d_bytes_per_step": bi,
+           "d2h_bytes_per_step": bo, "steps": n,
+           "returns": "verification outputs and loss to host memory (the heads stay resident on the device)"}
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())} (lmhead e2e)")
+    del hd, ht, wh, ws, hdd, htd
+    return {"ms": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12, "hidden": lw.hidden, "vocab": lw.vocab,
+            "e2e": e2e}
 
 
-def run_e2e(args, b, w, dev, af, torch, np):
+def run_e2e(args, b, w, dev, af, torch, np, grad_to_host=False):
     """Same step through the public API from pinned host buffers, copies inside the timed region.
 
-    Every step copies its inputs from pinned host memory and reads its results back.
+    Every step copies its inputs from pinned host memory and reads its results back:
+    the verification outputs and the loss, and with grad_to_host the float32 gradient
+    too (otherwise dz stays on the device, where an optimiser step would consume it).
     The copy of step i + 1 (on a copy stream, into the other of two device input
     buffers) overlaps the kernels of step i, as a serving loop would pipeline them.
     """
@@ -627,6 +802,8 @@ def run_e2e(args, b, w, dev, af, torch, np):
              "accept_rate": torch.empty(R, dtype=torch.float32).pin_memory(),
              "loss": torch.empty(1, dtype=torch.float32).pin_memory()}
     grad = torch.empty((Nd, w.vocab), dtype=torch.float32, device=dev)
+    if grad_to_host:
+        res_h["grad"] = torch.empty((Nd, w.vocab), dtype=torch.float32).pin_memory()
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     comp = torch.cuda.current_stream()
     copy_stream = torch.cuda.Stream()
@@ -672,6 +849,9 @@ def run_e2e(args, b, w, dev, af, torch, np):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": world * Nd * steps / el, "unit": "rows/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "steps": steps, "ms_per_step": el / steps * 1e3,
+            "returns": ("verification outputs, loss and the float32 gradient to host memory" if grad_to_host else
+                        "verification outputs and loss to host memory; the float32 gradient stays on the device "
+                        "for an on-device optimiser step"),
             "pipelined": "the copy of step i + 1 overlaps the kernels of step i (two device input buffers)"}
 
 

@@ -144,7 +144,7 @@ adaflash_status adaflash_verify_packed(const void* target_logits, adaflash_dtype
   p.target_argmax = target_argmax;
   p.status = d_status;
   // Target-only units read no draft row; the draft dtype only sizes the ring.
-  ADAFLASH_CUDA(launch_rowpass(p, 1, t_dtype, s));
+  ADAFLASH_CUDA(launch_rowpass(p, 1, t_dtype, rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)), s));
 
   FinalizeParams f = {};
   f.tokens = draft_tokens;
@@ -203,7 +203,9 @@ adaflash_status adaflash_opd_loss_fwd(const void* draft_logits, adaflash_dtype d
   p.ce_row = ce_row;
   p.row_stats = row_stats;
   p.status = d_status;
-  ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype, s));
+  const bool aligned = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
+                       rows_16b(target_logits, ld_t, dtype_bytes(t_dtype));
+  ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype, aligned, s));
 
   FinalizeParams f = {};
   f.tokens = draft_tokens;
@@ -263,7 +265,9 @@ adaflash_status adaflash_opd_loss_bwd(const void* draft_logits, adaflash_dtype d
   p.ld_g = ld_g;
   p.chunks_per_row = (vocab + kBwdChunk - 1) / kBwdChunk;
   p.status = d_status;
-  ADAFLASH_CUDA(launch_bwd(p, d_dtype, t_dtype, s));
+  const bool aligned = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
+                       rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)) && rows_16b(grad_draft, ld_g, 4);
+  ADAFLASH_CUDA(launch_bwd(p, d_dtype, t_dtype, aligned, s));
   return ADAFLASH_OK;
 }
 
@@ -329,12 +333,15 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
     const int row_bytes = vocab * (dtype_bytes(d_dtype) + dtype_bytes(t_dtype));
     p.cluster = rowpass_grad_cluster_size(vocab, p.N_d + p.R, row_bytes, num_sms());
     p.slice = rowpass_slice(vocab, p.cluster);
-    ADAFLASH_CUDA(launch_rowpass_grad(p, d_dtype, t_dtype, s));
+    ADAFLASH_CUDA(launch_rowpass_grad(p, d_dtype, t_dtype, aligned16, s));
   } else {
     // the streaming forward, then the streaming backward
     p.cluster = rowpass_cluster_size(vocab, p.N_d + p.R, num_sms());
     p.slice = rowpass_slice(vocab, p.cluster);
-    ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype, s));
+    ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype,
+                                 rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
+                                     rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)),
+                                 s));
   }
 
   FinalizeParams f = {};
@@ -375,7 +382,7 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
     b.ld_g = ld_g;
     b.chunks_per_row = (vocab + kBwdChunk - 1) / kBwdChunk;
     b.status = d_status;
-    ADAFLASH_CUDA(launch_bwd(b, d_dtype, t_dtype, s));
+    ADAFLASH_CUDA(launch_bwd(b, d_dtype, t_dtype, aligned16, s));
   }
   return ADAFLASH_OK;
 }

@@ -50,8 +50,9 @@ __device__ __forceinline__ float grad_entry(float z, float t, const RowCoef& k) 
 // body entries [H + c * kBwdChunk, ...)).  Target groups are then 16-byte words; the
 // draft row's groups sit 2 zs2 bytes past a boundary and are read with aligned loads
 // at that shift (one loop instance per shift); dz is stored at the gradient row's
-// own word offset.
-template <class DZ, class DT>
+// own word offset.  kShift = false: every row of z, t and dz is on the grid (the
+// shift-free instance, with less code).
+template <class DZ, class DT, bool kShift>
 __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams P) {
   __shared__ RowCoef s_coef;
   __shared__ int s_ok;
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams P) {
   const uint8_t* zrow = static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(d) * P.ld_z * DZ::kBytes;
   const uint8_t* trow = static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(s_trow) * P.ld_t * DT::kBytes;
   float* grow = P.grad + static_cast<int64_t>(d) * P.ld_g;
-  const RowGeom G = row_geom<DZ, DT>(zrow, trow, P.V);
+  const RowGeom G = row_geom<DZ, DT, kShift>(zrow, trow, P.V);
 
   const int b_begin = chunk * kBwdChunk;  // in the body
   const int b_end = min(P.V - G.H, b_begin + kBwdChunk);
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams P) {
   const uint32_t* tw = reinterpret_cast<const uint32_t*>(G.tb + static_cast<int64_t>(b_begin) * DT::kBytes);
   const uint8_t* zb = G.zb + static_cast<int64_t>(b_begin) * DZ::kBytes;
 
-  dispatch_shift<DZ>(G.zs2, [&](auto zs_c) {
+  dispatch_shift<DZ, kShift>(G.zs2, [&](auto zs_c) {
     constexpr int ZS = decltype(zs_c)::value;
     const uint32_t* zw = reinterpret_cast<const uint32_t*>(zb - 2 * ZS);  // the 16-byte boundary below
 #pragma unroll
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams P) {
         load8_shifted<DT, 0, true>(tw + off * DT::kBytes / 4, t);
 #pragma unroll
         for (int e = 0; e < 8; ++e) out[e] = grad_entry(z[e], t[e], k);
-        store8_stream(gbody + off, gq, out);
+        store8_stream<kShift>(gbody + off, gq, out);
       }
     }
   });
@@ -140,21 +141,26 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams P) {
   }
 }
 
-template <class DZ, class DT>
+template <class DZ, class DT, bool kShift>
 static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t s) {
   const long long blocks = static_cast<long long>(p.N_d) * p.chunks_per_row;
   if (blocks <= 0) return cudaSuccess;
   count_launch();
-  bwd_kernel<DZ, DT><<<static_cast<unsigned>(blocks), kBwdThreads, 0, s>>>(p);
+  bwd_kernel<DZ, DT, kShift><<<static_cast<unsigned>(blocks), kBwdThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, cudaStream_t s) {
+template <bool kShift>
+static cudaError_t launch_bwd_dtypes(const BwdParams& p, int z_dtype, int t_dtype, cudaStream_t s) {
   const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
-  if (zb && tb) return launch_bwd_t<BF16, BF16>(p, s);
-  if (!zb && tb) return launch_bwd_t<F32, BF16>(p, s);
-  if (zb && !tb) return launch_bwd_t<BF16, F32>(p, s);
-  return launch_bwd_t<F32, F32>(p, s);
+  if (zb && tb) return launch_bwd_t<BF16, BF16, kShift>(p, s);
+  if (!zb && tb) return launch_bwd_t<F32, BF16, kShift>(p, s);
+  if (zb && !tb) return launch_bwd_t<BF16, F32, kShift>(p, s);
+  return launch_bwd_t<F32, F32, kShift>(p, s);
+}
+
+cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool aligned, cudaStream_t s) {
+  return aligned ? launch_bwd_dtypes<false>(p, z_dtype, t_dtype, s) : launch_bwd_dtypes<true>(p, z_dtype, t_dtype, s);
 }
 
 }  // namespace adaflash

@@ -411,7 +411,13 @@ __device__ __forceinline__ void stcs_words(float* base, const float* x) {
 
 // Eight float32 results to dst (4-byte aligned, q = (dst / 4) mod 4 words past a
 // 16-byte boundary; q is uniform across a row, so the branch does not diverge).
+// kShift = false: dst is 16-byte aligned (q = 0).
+template <bool kShift = true>
 __device__ __forceinline__ void store8_stream(float* dst, int q, const float x[8]) {
+  if constexpr (!kShift) {
+    stcs_words<0, 8>(dst, x);
+    return;
+  }
   float* base = dst - q;
   switch (q) {
     case 1: stcs_words<1, 8>(base, x); break;
@@ -455,10 +461,13 @@ __device__ __forceinline__ void load8_shifted(const uint32_t* base, float x[8]) 
 }
 
 // Call f(IntC<zs2>{}) for a row's shift zs2 (in two-byte units, 0..7; only even
-// shifts occur for float32 rows, so only those are instantiated).
-template <class DT, class F>
+// shifts occur for float32 rows, so only those are instantiated).  kShift = false:
+// every row is on the grid, only the shift-0 instance exists.
+template <class DT, bool kShift = true, class F>
 __device__ __forceinline__ void dispatch_shift(int zs2, F&& f) {
-  if constexpr (DT::kBytes == 4) {
+  if constexpr (!kShift) {
+    f(IntC<0>{});
+  } else if constexpr (DT::kBytes == 4) {
     switch (zs2) {
       case 2: f(IntC<2>{}); break;
       case 4: f(IntC<4>{}); break;
@@ -490,9 +499,16 @@ struct RowGeom {
   const uint8_t* zb;  // draft body (may be off the grid), nullptr for a target-only row
 };
 
-template <class DZ, class DT>
+template <class DZ, class DT, bool kShift = true>
 __device__ __forceinline__ RowGeom row_geom(const uint8_t* zrow, const uint8_t* trow, int V) {
   RowGeom g;
+  if constexpr (!kShift) {  // every row on the grid
+    g.H = 0;
+    g.zs2 = 0;
+    g.tb = trow;
+    g.zb = zrow;
+    return g;
+  }
   const int off = static_cast<int>(reinterpret_cast<uintptr_t>(trow) & 15u);
   g.H = min(((16 - off) & 15) / DT::kBytes, V);
   g.tb = trow + static_cast<int64_t>(g.H) * DT::kBytes;

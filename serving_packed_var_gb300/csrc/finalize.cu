@@ -22,11 +22,11 @@ constexpr int kFinThreads = 1024;
 
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizeParams P) {
   // Launched as a programmatic dependent of the row pass: wait until its writes
-  // (target_argmax, kl_row, ce_row) are complete and visible.
+  // (target_argmax, kl_row, ce_row) are complete and visible.  This grid releases
+  // the next call's row pass only when it exits: released right after the wait, the
+  // next persistent row pass was launched while these 1024-thread blocks still held
+  // SMs, and on a 512-request batch the call took 3.63 ms instead of 2.51 ms.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // The next call's row pass may be scheduled now; it waits for this grid's
-  // completion before touching global memory.
-  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * kFinThreads + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * kFinThreads) >> 5;

@@ -130,15 +130,17 @@ void count_launch();
 
 // dtype codes match adaflash_dtype (0 = fp32, 1 = bf16)
 // The row pass (rows at any element-aligned address: each row follows its target
-// row's 16-byte grid).
-cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s);
+// row's 16-byte grid).  aligned: every row of z and t (and of the gradient) starts on
+// the 16-byte grid, which selects the smaller shift-free instance.
+cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool aligned, cudaStream_t s);
 // The row pass with the gradient (single-pass forward + backward, any element-aligned
 // rows).  Cluster size: rowpass_grad_cluster_size (row_bytes = V (b_z + b_t)).
-cudaError_t launch_rowpass_grad(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s);
+cudaError_t launch_rowpass_grad(const RowPassParams& p, int z_dtype, int t_dtype, bool aligned, cudaStream_t s);
 int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int num_sms);
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
-// The backward (rows at any element-aligned address).
-cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, cudaStream_t s);
+// The backward (rows at any element-aligned address; aligned: every row of z, t and
+// dz on the 16-byte grid, the shift-free instance).
+cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool aligned, cudaStream_t s);
 // Fused forward + backward (K4).  fused_max_units is the largest batch (draft rows +
 // requests) the fused kernel is used for: 0 when a row pair does not fit a cluster's
 // shared memory; above it the caller runs K1 + K3, which stream faster on full waves.

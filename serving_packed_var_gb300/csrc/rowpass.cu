@@ -161,7 +161,10 @@ __device__ __forceinline__ float grad_of(float z, float t, const RowGrad& k) {
 // target body is bulk-copied as it lies; the draft body, which may start 2 zs2
 // bytes past a boundary, is bulk-copied from the boundary below it (16 bytes more)
 // and read with aligned loads at that shift (one instance of the loop per shift).
-template <class DZ, class DT, bool kGrad>
+// kShift = false is the instance for batches whose every row (and gradient row) starts
+// on the 16-byte grid: no head, no shifted loads, plain 16-byte stores; its smaller
+// code runs the aligned batch 6% faster than the general instance does.
+template <class DZ, class DT, bool kGrad, bool kShift>
 __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBlocks)
     rowpass_kernel(const RowPassParams P) {
   constexpr int kConsumerWarps = RowCfg<kGrad>::kWarps;
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
             U.pair ? static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(U.d) * P.ld_z * DZ::kBytes : nullptr;
         const uint8_t* trow =
             static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(max(U.s, 0)) * P.ld_t * DT::kBytes;
-        const RowGeom G = row_geom<DZ, DT>(zrow, trow, P.V);
+        const RowGeom G = row_geom<DZ, DT, kShift>(zrow, trow, P.V);
         const int v_begin = static_cast<int>(rank) * P.slice;  // in the body
         const int v_end = U.bad ? v_begin : min(P.V - G.H, v_begin + P.slice);
         const int body = max(0, v_end - v_begin) & ~7;
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
           U.pair ? static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(U.d) * P.ld_z * DZ::kBytes : nullptr;
       const uint8_t* trow =
           static_cast<const uint8_t*>(P.t) + static_cast<int64_t>(max(U.s, 0)) * P.ld_t * DT::kBytes;
-      const RowGeom G = row_geom<DZ, DT>(zrow, trow, P.V);
+      const RowGeom G = row_geom<DZ, DT, kShift>(zrow, trow, P.V);
       const int Vb = P.V - G.H;
       const int v_begin = static_cast<int>(rank) * P.slice;  // in the body
       const int v_end = U.bad ? v_begin : min(Vb, v_begin + P.slice);
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
       acc_init(acc);
       if (U.pair) {
         // The draft body's shift picks the loop instance (uniform per unit).
-        dispatch_shift<DZ>(G.zs2, [&](auto zs_c) {
+        dispatch_shift<DZ, kShift>(G.zs2, [&](auto zs_c) {
           constexpr int ZS = decltype(zs_c)::value;
           for (int e0 = 0; e0 < body; e0 += kChunk, ++cc) {
             const int st = static_cast<int>(cc % kStages);
@@ -639,7 +642,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
           float* gbody = grow + G.H + v_begin;                          // this slice of the body
           const int gq = static_cast<int>((reinterpret_cast<uintptr_t>(gbody) >> 2) & 3u);
           const int nch = (body + kChunk - 1) / kChunk;
-          dispatch_shift<DZ>(G.zs2, [&](auto zs_c) {
+          dispatch_shift<DZ, kShift>(G.zs2, [&](auto zs_c) {
             constexpr int ZS = decltype(zs_c)::value;
             for (int ci = 0; ci < nch; ++ci, ++cc) {
               const int e0 = kReverseP2 ? (nch - 1 - ci) * kChunk : ci * kChunk;
@@ -661,7 +664,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
                   load8_smem<DT>(stage, g, t, vm);
 #pragma unroll
                   for (int e = 0; e < 8; ++e) out[e] = grad_of(z[e], t[e], k);
-                  store8_stream(gbody + e0 + (g << 3), gq, out);
+                  store8_stream<kShift>(gbody + e0 + (g << 3), gq, out);
                 }
               }
               // The group holding the first max of t: the thread that just wrote it finds
@@ -798,9 +801,9 @@ static size_t rowpass_smem(int slice) {
 }
 
 // Co-resident clusters of this kernel at this cluster size (cached).
-template <class DZ, class DT, bool kGrad>
+template <class DZ, class DT, bool kGrad, bool kShift>
 static int active_clusters(int cluster, size_t smem) {
-  auto kern = rowpass_kernel<DZ, DT, kGrad>;
+  auto kern = rowpass_kernel<DZ, DT, kGrad, kShift>;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return 1;
   // The query must see the shared-memory size the launch will use.
@@ -834,15 +837,15 @@ static int active_clusters(int cluster, size_t smem) {
 }
 
 // One launch over units [p.unit_begin, p.unit_end), persistent clusters.
-template <class DZ, class DT, bool kGrad>
+template <class DZ, class DT, bool kGrad, bool kShift>
 static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaStream_t stream) {
   const size_t smem = rowpass_smem<DZ, DT, kGrad>(p.slice);
-  auto kern = rowpass_kernel<DZ, DT, kGrad>;
+  auto kern = rowpass_kernel<DZ, DT, kGrad, kShift>;
   const int units = p.unit_end - p.unit_begin;
   if (units <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int clusters = active_clusters<DZ, DT, kGrad>(p.cluster, smem);
+  const int clusters = active_clusters<DZ, DT, kGrad, kShift>(p.cluster, smem);
   cudaLaunchConfig_t cfg = {};
   const int grid_clusters = units < clusters ? units : clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters) * static_cast<unsigned>(p.cluster), 1, 1);
@@ -870,7 +873,7 @@ static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaS
 // Every launch is programmatic: the first one waits for the stream's previous
 // kernel before touching global memory; a second one starts as CTAs of the first
 // retire and completes only after the first.
-template <class DZ, class DT, bool kGrad = false>
+template <class DZ, class DT, bool kGrad, bool kShift>
 static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   const int units = (p0.mode == kModeVerify) ? p0.N_t : (p0.N_d + p0.R);
   if (units <= 0) return cudaSuccess;
@@ -878,16 +881,16 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   p.unit_begin = 0;
   p.unit_end = units;
   p.wait_prior = 0;
-  const int clusters = active_clusters<DZ, DT, kGrad>(p.cluster, rowpass_smem<DZ, DT, kGrad>(p.slice));
+  const int clusters = active_clusters<DZ, DT, kGrad, kShift>(p.cluster, rowpass_smem<DZ, DT, kGrad>(p.slice));
   const int split = (units / clusters) * clusters;
   // With the gradient, a last partial wave of target-only rows (cheap: no second pass)
   // stays in the one launch rather than costing a launch of its own.
   if (!ADAFLASH_ROWPASS_TAIL || units <= clusters || split == units || p.cluster >= kMaxCluster ||
       (kGrad && p0.mode == kModeFwd && split >= p0.N_d))
-    return launch_range<DZ, DT, kGrad>(p, true, stream);
+    return launch_range<DZ, DT, kGrad, kShift>(p, true, stream);
   const RowPassParams base = p;
   p.unit_end = split;
-  cudaError_t e = launch_range<DZ, DT, kGrad>(p, true, stream);
+  cudaError_t e = launch_range<DZ, DT, kGrad, kShift>(p, true, stream);
   if (e != cudaSuccess) return e;
   auto launch_tail = [&](int b, int end) {
     RowPassParams tail = base;
@@ -905,7 +908,7 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
     }
     if (tail.cluster < p.cluster) tail.cluster = p.cluster;
     tail.slice = rowpass_slice(p.V, tail.cluster);
-    return launch_range<DZ, DT, kGrad>(tail, true, stream);
+    return launch_range<DZ, DT, kGrad, kShift>(tail, true, stream);
   };
   // With the gradient, leftover paired rows and the cheap target-only rows get their
   // own launches, so the few expensive rows are split over the larger clusters their
@@ -933,20 +936,22 @@ int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int num_sms) 
   return c;
 }
 
-cudaError_t launch_rowpass_grad(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s) {
+template <bool kGrad, bool kShift>
+static cudaError_t launch_dtypes(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s) {
   const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
-  if (zb && tb) return launch_one<BF16, BF16, true>(p, s);
-  if (!zb && tb) return launch_one<F32, BF16, true>(p, s);
-  if (zb && !tb) return launch_one<BF16, F32, true>(p, s);
-  return launch_one<F32, F32, true>(p, s);
+  if (zb && tb) return launch_one<BF16, BF16, kGrad, kShift>(p, s);
+  if (!zb && tb) return launch_one<F32, BF16, kGrad, kShift>(p, s);
+  if (zb && !tb) return launch_one<BF16, F32, kGrad, kShift>(p, s);
+  return launch_one<F32, F32, kGrad, kShift>(p, s);
 }
 
-cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, cudaStream_t s) {
-  const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
-  if (zb && tb) return launch_one<BF16, BF16>(p, s);
-  if (!zb && tb) return launch_one<F32, BF16>(p, s);
-  if (zb && !tb) return launch_one<BF16, F32>(p, s);
-  return launch_one<F32, F32>(p, s);
+cudaError_t launch_rowpass_grad(const RowPassParams& p, int z_dtype, int t_dtype, bool aligned, cudaStream_t s) {
+  return aligned ? launch_dtypes<true, false>(p, z_dtype, t_dtype, s) : launch_dtypes<true, true>(p, z_dtype, t_dtype, s);
+}
+
+cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, bool aligned, cudaStream_t s) {
+  return aligned ? launch_dtypes<false, false>(p, z_dtype, t_dtype, s)
+                 : launch_dtypes<false, true>(p, z_dtype, t_dtype, s);
 }
 
 }  // namespace adaflash
