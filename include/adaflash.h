@@ -271,12 +271,19 @@ adaflash_status adaflash_lmhead_opd_fwd(
  * library, which every GPU that loads the library's LM-head code holds until the
  * process exits.
  *
- * Arguments, outputs and results are those of adaflash_lmhead_opd_fwd.  A batch whose
+ * Arguments, outputs and results are those of adaflash_lmhead_opd_fwd, and bad
+ * arguments get the same status from both.  A batch whose
  * adaflash_lmhead_workspace_bytes(R, N_d, V, H) exceeds the array is rejected with
  * ADAFLASH_ERR_UNSUPPORTED before anything is enqueued.  The first call on a device
  * looks up the array's device address with that device current (set-up done once
- * per device); make that first call before any stream capture.  Nothing here calls
- * cudaMalloc or cudaFree.  All calls share the one array and each leaves its contents
+ * per device); make that first call before any stream capture.  The array's device
+ * memory is committed when the library's LM-head code is loaded on the device: with
+ * CUDA's lazy module loading (the default) that is this first call, so make it
+ * outside any region where the device may not allocate (a failure there returns
+ * ADAFLASH_ERR_CUDA).  The address looked up is kept for the life of the process:
+ * cudaDeviceReset, or destroying and recreating the device's primary context,
+ * invalidates it, and this entry point is not supported after either.  Nothing here
+ * calls cudaMalloc or cudaFree.  All calls share the one array and each leaves its contents
  * behind: a call writes every scratch byte it reads before reading it, so nothing is
  * cleared, but calls whose kernels overlap on the GPU (other streams, other host
  * threads) race on the array and must be serialised by the caller.

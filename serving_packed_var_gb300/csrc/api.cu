@@ -440,14 +440,17 @@ adaflash_status adaflash_lmhead_logits(const void* hidden_rows, int64_t ld_h, in
   return ADAFLASH_OK;
 }
 
-adaflash_status adaflash_lmhead_opd_fwd(const void* draft_hidden, int64_t ld_hd, const void* target_hidden,
-                                        int64_t ld_ht, const void* draft_head, int64_t ld_wd, const void* target_head,
-                                        int64_t ld_wt, int32_t hidden, const int32_t* draft_tokens,
-                                        const int32_t* draft_offsets, int32_t num_requests, int32_t num_draft_rows,
-                                        int32_t vocab, float clip_c, float ce_weight, void* workspace,
-                                        int64_t workspace_bytes, int32_t* target_argmax, int32_t* accept_len,
-                                        int32_t* bonus_token, float* accept_rate, float* kl_row, float* ce_row,
-                                        float* row_stats, float* loss, uint32_t* d_status, void* stream) {
+}  // extern "C"
+
+namespace {
+// Argument checks shared by the logit-free entry points (everything but the scratch).
+adaflash_status check_lmhead_fwd_args(const void* draft_hidden, int64_t ld_hd, const void* target_hidden,
+                                      int64_t ld_ht, const void* draft_head, int64_t ld_wd, const void* target_head,
+                                      int64_t ld_wt, int32_t hidden, const int32_t* draft_tokens,
+                                      const int32_t* draft_offsets, int32_t num_requests, int32_t num_draft_rows,
+                                      int32_t vocab, float clip_c, float ce_weight, int32_t* target_argmax,
+                                      int32_t* accept_len, int32_t* bonus_token, float* accept_rate, float* kl_row,
+                                      float* ce_row, float* row_stats, float* loss, uint32_t* d_status) {
   ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
   if (hidden < 64 || hidden % 64 != 0) return ADAFLASH_ERR_INVALID_ARG;
   ADAFLASH_TRY(check_bf16_rows(draft_hidden, ld_hd, hidden));
@@ -460,6 +463,24 @@ adaflash_status adaflash_lmhead_opd_fwd(const void* draft_hidden, int64_t ld_hd,
     return ADAFLASH_ERR_INVALID_ARG;
   if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
   if (!(clip_c > 0.0f) || !std::isfinite(ce_weight)) return ADAFLASH_ERR_INVALID_ARG;
+  return ADAFLASH_OK;
+}
+}  // namespace
+
+extern "C" {
+
+adaflash_status adaflash_lmhead_opd_fwd(const void* draft_hidden, int64_t ld_hd, const void* target_hidden,
+                                        int64_t ld_ht, const void* draft_head, int64_t ld_wd, const void* target_head,
+                                        int64_t ld_wt, int32_t hidden, const int32_t* draft_tokens,
+                                        const int32_t* draft_offsets, int32_t num_requests, int32_t num_draft_rows,
+                                        int32_t vocab, float clip_c, float ce_weight, void* workspace,
+                                        int64_t workspace_bytes, int32_t* target_argmax, int32_t* accept_len,
+                                        int32_t* bonus_token, float* accept_rate, float* kl_row, float* ce_row,
+                                        float* row_stats, float* loss, uint32_t* d_status, void* stream) {
+  ADAFLASH_TRY(check_lmhead_fwd_args(draft_hidden, ld_hd, target_hidden, ld_ht, draft_head, ld_wd, target_head, ld_wt,
+                                     hidden, draft_tokens, draft_offsets, num_requests, num_draft_rows, vocab, clip_c,
+                                     ce_weight, target_argmax, accept_len, bonus_token, accept_rate, kl_row, ce_row,
+                                     row_stats, loss, d_status));
   const int64_t need = adaflash_lmhead_workspace_bytes(num_requests, num_draft_rows, vocab, hidden);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return ADAFLASH_ERR_INVALID_ARG;
   ADAFLASH_TRY(check_device());
@@ -538,6 +559,11 @@ adaflash_status adaflash_lmhead_opd_fwd_static(const void* draft_hidden, int64_t
                                                int32_t* accept_len, int32_t* bonus_token, float* accept_rate,
                                                float* kl_row, float* ce_row, float* row_stats, float* loss,
                                                uint32_t* d_status, void* stream) {
+  // the same argument checks as the workspace entry point, then the array's size
+  ADAFLASH_TRY(check_lmhead_fwd_args(draft_hidden, ld_hd, target_hidden, ld_ht, draft_head, ld_wd, target_head, ld_wt,
+                                     hidden, draft_tokens, draft_offsets, num_requests, num_draft_rows, vocab, clip_c,
+                                     ce_weight, target_argmax, accept_len, bonus_token, accept_rate, kl_row, ce_row,
+                                     row_stats, loss, d_status));
   const int64_t need = adaflash_lmhead_workspace_bytes(num_requests, num_draft_rows, vocab, hidden);
   if (need < 0) return ADAFLASH_ERR_INVALID_ARG;
   if (need > ADAFLASH_LMHEAD_STATIC_SCRATCH_BYTES) return ADAFLASH_ERR_UNSUPPORTED;

@@ -154,3 +154,28 @@ def test_python_binding_refuses_cpu_tensors():
     t = torch.zeros(2, 8)
     with pytest.raises(ValueError):
         af.adaflash_verify_packed(t, torch.zeros(1, dtype=torch.int32), torch.zeros(2, dtype=torch.int32))
+
+
+def _lmhead(lib, static, **kw):
+    a = dict(hd=FAKE, ldhd=256, ht=FAKE, ldht=256, wd=FAKE, ldwd=256, wt=FAKE, ldwt=256, H=256, tok=FAKE, doff=FAKE,
+             R=4, Nd=29, V=2048, c=1.0, beta=1.0, loss=FAKE, kl=FAKE, status=None)
+    a.update(kw)
+    head = (a["hd"], a["ldhd"], a["ht"], a["ldht"], a["wd"], a["ldwd"], a["wt"], a["ldwt"], a["H"], a["tok"],
+            a["doff"], a["R"], a["Nd"], a["V"], a["c"], a["beta"])
+    outs = (FAKE, FAKE, FAKE, FAKE, a["kl"], FAKE, FAKE, a["loss"], a["status"], None)
+    if static:
+        return lib.adaflash_lmhead_opd_fwd_static(*head, *outs)
+    return lib.adaflash_lmhead_opd_fwd(*head, FAKE, 1 << 40, *outs)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(hd=None), dict(wt=None), dict(hd=FAKE + 8), dict(ldhd=100), dict(ldwd=260), dict(H=100), dict(H=32),
+    dict(tok=None), dict(doff=FAKE + 2), dict(loss=None), dict(kl=FAKE + 1), dict(c=0.0), dict(c=float("nan")),
+    dict(beta=float("inf")), dict(Nd=3), dict(R=-1), dict(status=FAKE + 2),
+    # oversized for the static array as well as invalid: the argument error wins
+    dict(R=128, Nd=2000, V=524288, H=4096, ldhd=4096, ldht=4096, ldwd=4096, ldwt=4096, tok=None),
+])
+def test_lmhead_entry_points_reject_alike(lib, kw):
+    """The static-scratch entry point reports the same status as the workspace one for bad arguments."""
+    assert _lmhead(lib, False, **kw) == INVALID
+    assert _lmhead(lib, True, **kw) == INVALID
