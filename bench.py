@@ -196,7 +196,24 @@ K_MIX = {
 
 def workload_text(w):
     return (f"{w.name}: concurrency {w.num_requests}, V={w.vocab}, {w.d_dtype} draft / {w.t_dtype} target, "
-            f"{K_MIX.get(w.name, 'k_i as generated')}, clip c={w.clip_c}")
+            f"{K_MIX.get(w.name.split('[')[0], 'k_i as generated')}, clip c={w.clip_c}")
+
+
+def workload_from_args(args, make_workload, seed=0):
+    """The named workload, or its first --requests requests (same rows, same planted structure)."""
+    import numpy as np
+    w = make_workload(args.workload, seed=seed)
+    n = getattr(args, "requests", 0)
+    if n and n < w.num_requests:
+        nd = int(np.sum(w.k[:n]))
+        nt = nd + n
+        over = dict(k=w.k[:n], planted_accept=w.planted_accept[:n])
+        for key, lim in (("clip_rows", nd), ("equal_rows", nd), ("tie_rows", nt), ("constant_target_rows", nt)):
+            rows = getattr(w, key)
+            over[key] = rows[rows < lim]
+        w = make_workload(args.workload, seed=seed, **over)
+        w.name = f"{args.workload}[:{n}]"
+    return w
 
 
 def workload_config(w):
@@ -270,7 +287,7 @@ def run_ours(args):
         build()
     barrier()
 
-    w = make_workload(args.workload, seed=rank)
+    w = workload_from_args(args, make_workload, seed=rank)
     b = materialize(w)
     Nd, R = w.num_draft_rows, w.num_requests
 
@@ -382,6 +399,12 @@ def run_ours(args):
         raise RuntimeError(f"device status {int(status.item())}")
 
     # cold-HBM per-call times: an L2-sized flush (twice the L2) before every call
+    if args.profile_only:
+        # a profiling run: the warm-up, the timed steps, the separate calls, verification
+        # and sampled verification only
+        print(json.dumps({"profile_only": True, "workload": workload_text(w), "ms_per_step": ms_local / K,
+                          "launches": launches}), flush=True)
+        return
     cold = run_cold(w, dev, af, torch, np, z, t, tok, doff, status, out, grad, stream, fbo)
 
     # concurrency 1 (one request of 16 draft rows): the step eager and replayed from a CUDA graph
@@ -864,7 +887,7 @@ def run_reference(args):
     if rank != 0:
         return
     from synth import make_workload, materialize
-    w = make_workload(args.workload, seed=0)
+    w = workload_from_args(args, make_workload, seed=0)
     b = materialize(w)
     base = None
     for _ in range(args.warmup):
@@ -893,6 +916,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c128")
     ap.add_argument("--no-lmhead", action="store_true", help="skip the logit-free (hidden-state) measurement")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="take only the first N requests of the workload (a smaller case of the same shape)")
+    ap.add_argument("--profile-only", action="store_true",
+                    help="warm-up, timed steps and the separate calls only; prints a short JSON line (for ncu)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":

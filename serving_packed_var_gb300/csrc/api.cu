@@ -79,6 +79,18 @@ int num_sms() {
   return n;
 }
 
+// L2 size of the current device in bytes (cached per device; 0 if unknown).
+long long l2_bytes() {
+  static long long cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n < 1) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
 #define ADAFLASH_TRY(expr)                          \
   do {                                              \
     const adaflash_status st_ = (expr);             \
@@ -331,7 +343,8 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
     ADAFLASH_CUDA(launch_fused(p, d_dtype, t_dtype, num_sms(), s));
   } else if (stream_grad) {
     const int row_bytes = vocab * (dtype_bytes(d_dtype) + dtype_bytes(t_dtype));
-    p.cluster = rowpass_grad_cluster_size(vocab, p.N_d + p.R, row_bytes, num_sms());
+    p.cluster = rowpass_grad_cluster_size(vocab, p.N_d + p.R, row_bytes, rowpass_grad_chunk(d_dtype, t_dtype),
+                                          num_sms(), l2_bytes());
     p.slice = rowpass_slice(vocab, p.cluster);
     ADAFLASH_CUDA(launch_rowpass_grad(p, d_dtype, t_dtype, aligned16, s));
   } else {

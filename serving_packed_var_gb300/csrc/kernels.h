@@ -136,7 +136,8 @@ cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, boo
 // The row pass with the gradient (single-pass forward + backward, any element-aligned
 // rows).  Cluster size: rowpass_grad_cluster_size (row_bytes = V (b_z + b_t)).
 cudaError_t launch_rowpass_grad(const RowPassParams& p, int z_dtype, int t_dtype, bool aligned, cudaStream_t s);
-int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int num_sms);
+int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int chunk_entries, int num_sms, long long l2_bytes);
+int rowpass_grad_chunk(int z_dtype, int t_dtype);  // vocabulary entries per ring stage
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
 // The backward (rows at any element-aligned address; aligned: every row of z, t and
 // dz on the 16-byte grid, the shift-free instance).

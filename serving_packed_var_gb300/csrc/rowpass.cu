@@ -43,6 +43,7 @@
 // "On-Policy Distillation (OPD) for Domain Adaptation" (reverse KL, top-1 hard
 // label, per-vocabulary clipping) and the opening section (the target verifies the
 // draft; its argmax is the greedy choice).
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 #include <cmath>
@@ -921,19 +922,27 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   return launch_tail(split, units);
 }
 
-#ifndef ADAFLASH_FWDBWD_L2_BUDGET
-#define ADAFLASH_FWDBWD_L2_BUDGET (64ll << 20)  // bytes of rows in flight in the single-pass forward + backward
-#endif
-
-int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int num_sms) {
-  // The row pass's size, raised until the rows in flight at once (resident CTAs /
-  // C rows of row_bytes) fit the L2 budget, so that the second pass over each slice
-  // is served from L2.
+int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int chunk_entries, int num_sms, long long l2_bytes) {
+  // The row pass's size, then at least 6 CTAs while each CTA's slice still holds four
+  // ring chunks (C = 6 measured best on GB300 for bf16 rows and for fp32-draft /
+  // bf16-target rows at V = 151936, against 4, 5, 7 and 8: more CTAs per row make the
+  // per-row exchanges more frequent per byte, fewer put more rows in flight), then
+  // raised until the rows in flight at once (resident CTAs / C rows of row_bytes) fit
+  // three quarters of the L2, so that the second pass over each slice is served from L2.
   int c = rowpass_cluster_size(vocab, units, num_sms);
-  while (c < kMaxCluster && static_cast<long long>(RowCfg<true>::kMinBlocks) * num_sms / c * row_bytes >
-                                ADAFLASH_FWDBWD_L2_BUDGET)
-    ++c;
+  const int floor_c = std::min(6, std::max(1, vocab / (4 * chunk_entries)));
+  if (c < floor_c) c = floor_c;
+  const long long budget = (l2_bytes > 0 ? l2_bytes : (126ll << 20)) * 3 / 4;
+  while (c < kMaxCluster && static_cast<long long>(RowCfg<true>::kMinBlocks) * num_sms / c * row_bytes > budget) ++c;
   return c;
+}
+
+int rowpass_grad_chunk(int z_dtype, int t_dtype) {
+  const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
+  if (zb && tb) return chunk_of<BF16, BF16, true>();
+  if (!zb && tb) return chunk_of<F32, BF16, true>();
+  if (zb && !tb) return chunk_of<BF16, F32, true>();
+  return chunk_of<F32, F32, true>();
 }
 
 template <bool kGrad, bool kShift>
