@@ -26,14 +26,24 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
   // the next call's row pass only when it exits: released right after the wait, the
   // next persistent row pass was launched while these 1024-thread blocks still held
   // SMs, and on a 512-request batch the call took 3.63 ms instead of 2.51 ms.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * kFinThreads + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * kFinThreads) >> 5;
 
+  // The offsets and the tokens are inputs the row pass does not write: the first
+  // request's are read before waiting for it.
+  int d0 = 0, d1 = 0, tok = 0;
+  auto load_inputs = [&](int r) {
+    d0 = __ldg(P.doff + r);
+    d1 = __ldg(P.doff + r + 1);
+    const int k = d1 - d0;
+    tok = (lane < k && k <= ADAFLASH_MAX_K && d0 >= 0 && d1 <= P.N_d) ? __ldg(P.tokens + d0 + lane) : 0;
+  };
+  if (gwarp < P.R) load_inputs(gwarp);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   for (int i = gwarp; i < P.R; i += nwarps) {
-    const int d0 = __ldg(P.doff + i);
-    const int d1 = __ldg(P.doff + i + 1);
+    if (i != gwarp) load_inputs(i);
     const int k = d1 - d0;
     bool ok = (k >= 1) && (k <= ADAFLASH_MAX_K) && (d0 >= 0) && (d1 <= P.N_d);
     if (i == 0 && d0 != 0) ok = false;
@@ -47,19 +57,21 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const FinalizePar
       }
       continue;
     }
+    // lanes 0..k read the target's choice at the request's k + 1 positions (the last one
+    // is the bonus position), so the bonus token is a shuffle, not a second load
+    const int a = lane <= k ? __ldg(P.target_argmax + d0 + i + lane) : -1;
     bool mismatch = false, badtok = false;
     if (lane < k) {
-      const int tok = __ldg(P.tokens + d0 + lane);
-      const int a = __ldg(P.target_argmax + d0 + i + lane);
       badtok = (tok < 0) || (tok >= P.V);
       mismatch = badtok || (tok != a);
     }
     const unsigned mm = __ballot_sync(0xffffffffu, mismatch);
     const unsigned bt = __ballot_sync(0xffffffffu, badtok);
+    const int L = mm ? (__ffs(mm) - 1) : k;
+    const int bonus = __shfl_sync(0xffffffffu, a, L);
     if (lane == 0) {
-      const int L = mm ? (__ffs(mm) - 1) : k;
       P.accept_len[i] = L;
-      P.bonus_token[i] = __ldg(P.target_argmax + d0 + i + L);
+      P.bonus_token[i] = bonus;
       P.accept_rate[i] = __fdiv_rn(static_cast<float>(L), static_cast<float>(k));
       if (bt) flag_status(P.status, ADAFLASH_ERR_BAD_TOKEN);
     }
