@@ -667,6 +667,14 @@ def run_configs(dev, af, torch, np, stream, peak, make_workload, materialize):
                 af.adaflash_verify_packed(t, tok, doff, out=vo["v"], status=st)
             e["verify_packed"] = _entry(_back_to_back(torch, stream, verify, n),
                                         w.num_target_rows * w.bytes_per_target_elem * V, Nd, peak)
+            urng = np.random.default_rng(2000)
+            u_acc = torch.from_numpy(urng.random(Nd, dtype=np.float32)).to(dev)
+            u_smp = torch.from_numpy(urng.random(R, dtype=np.float32)).to(dev)
+            so = {"s": af.adaflash_verify_sampled(z, t, tok, doff, SAMPLED_T, u_acc, u_smp, status=st)}
+
+            def sampled():
+                af.adaflash_verify_sampled(z, t, tok, doff, SAMPLED_T, u_acc, u_smp, out=so["s"], status=st)
+            e["sampled_verify"] = _entry(_back_to_back(torch, stream, sampled, n), fb, Nd, peak)
         torch.cuda.synchronize()
         if int(st.item()) != 0:
             raise RuntimeError(f"device status {int(st.item())} ({name})")

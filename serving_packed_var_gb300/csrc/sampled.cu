@@ -111,7 +111,8 @@ __device__ __forceinline__ void unpack16(const uint4& w, float (&x)[8]) {
 }
 
 // Eight consecutive entries starting at v0 (a multiple of 8); 16-byte loads when
-// the row starts on a 16-byte boundary, else eight element loads.
+// the row starts on a 16-byte boundary, else eight element loads (the few groups
+// left after the unrolled loops, and the draw's re-reads).
 template <class DT>
 __device__ __forceinline__ void load8(const uint8_t* row, bool aligned16, int v0, float (&x)[8]) {
   if (!aligned16) {
@@ -179,14 +180,23 @@ __device__ MaxSum slice_maxsum(const uint8_t* row, int V, int rank, int C, float
       }
     }
   } else {
-    // rows off the 16-byte grid: element loads, two groups in flight per thread
-    for (; g + B < g1; g += 2 * B) {
-      float x[2][8];
-      load8<DT>(row, false, g << 3, x[0]);
-      load8<DT>(row, false, (g + B) << 3, x[1]);
-      ms_add_group<8>(a, x[0], scale);
-      ms_add_group<8>(a, x[1], scale);
-    }
+    // rows off the 16-byte grid: the same groups (so the same order of operations),
+    // each read with the widest aligned loads at the row's byte shift, one loop
+    // instance per shift, several groups in flight per thread
+    const int zs2 = static_cast<int>((reinterpret_cast<uintptr_t>(row) & 15u) >> 1);
+    dispatch_shift<DT>(zs2, [&](auto zs_c) {
+      constexpr int ZS = decltype(zs_c)::value;
+      constexpr int U = DT::kBytes == 2 ? 4 : 2;
+      const uint32_t* base = reinterpret_cast<const uint32_t*>(row - 2 * ZS);  // the 16-byte boundary below
+      for (; g + (U - 1) * B < g1; g += U * B) {
+        float x[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          load8_shifted<DT, ZS, true>(base + static_cast<int64_t>(g + u * B) * 2 * DT::kBytes, x[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) ms_add_group<8>(a, x[u], scale);
+      }
+    });
   }
   for (; g < g1; g += B) {
     float x[8];
