@@ -32,18 +32,16 @@ namespace adaflash {
 
 namespace {
 
-#ifndef ADAFLASH_FUSED_THREADS
-#define ADAFLASH_FUSED_THREADS 256
-#endif
-constexpr int kFThreads = ADAFLASH_FUSED_THREADS;  // a power of two
+constexpr int kFThreads = 256;  // a power of two
 constexpr int kFWarps = kFThreads / 32;
 constexpr uint32_t kPiece = 16384;  // bytes per bulk copy
-#ifndef ADAFLASH_FUSED_MAX_WAVES
-#define ADAFLASH_FUSED_MAX_WAVES 1  // the fused kernel takes batches of at most this many waves of units
-#endif
-#ifndef ADAFLASH_FUSED_CTAS_PER_SM
-#define ADAFLASH_FUSED_CTAS_PER_SM 2  // shared-memory budget: this many resident CTAs per SM
-#endif
+// The shared-memory budget: two resident CTAs per SM (a slice of a bf16 pair at
+// V = 151936 then needs clusters of 6).
+constexpr int kFCtasPerSm = 2;
+// The fused kernel takes batches of at most one wave of row units: beyond that its
+// phases, one after another inside each CTA, leave the HBM stream idle (a 128-request
+// batch at V = 151936: 384 us, against 219.8 us for the row pass with the gradient).
+constexpr int kFMaxWaves = 1;
 constexpr size_t kSmemPerSm = 227 * 1024;
 constexpr size_t kStaticReserve = 4096;  // static shared memory and the per-CTA reservation
 
@@ -85,7 +83,7 @@ __host__ __device__ constexpr size_t fused_smem(int slice) {
 }  // namespace
 
 template <class DZ, class DT>
-__global__ void __launch_bounds__(kFThreads, ADAFLASH_FUSED_CTAS_PER_SM) fused_kernel(const RowPassParams P) {
+__global__ void __launch_bounds__(kFThreads, kFCtasPerSm) fused_kernel(const RowPassParams P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar;
   __shared__ uint64_t part_bar[2];
@@ -442,11 +440,11 @@ FOcc g_focc[64];
 int g_focc_n = 0;
 }  // namespace
 
-// Smallest cluster whose slices fit the shared-memory budget of
-// ADAFLASH_FUSED_CTAS_PER_SM CTAs per SM (else of one CTA per SM); 0 when even 8 do not fit.
+// Smallest cluster whose slices fit the shared-memory budget of kFCtasPerSm CTAs per
+// SM (else of one CTA per SM); 0 when even 8 do not fit.
 int fused_cluster_size(int vocab, int bytes_per_entry) {
   for (int pass = 0; pass < 2; ++pass) {
-    const size_t budget = (pass == 0 ? kSmemPerSm / ADAFLASH_FUSED_CTAS_PER_SM : kSmemPerSm) - kStaticReserve;
+    const size_t budget = (pass == 0 ? kSmemPerSm / kFCtasPerSm : kSmemPerSm) - kStaticReserve;
     for (int c = 1; c <= kMaxCluster; ++c) {
       const int slice = rowpass_slice(vocab, c);
       // z and t share the slice; round128 of the z part adds at most 128 bytes
@@ -495,8 +493,7 @@ template <class DZ, class DT>
 static int fused_max_units_t(int vocab, int num_sms) {
   const int C = fused_cluster_size(vocab, DZ::kBytes + DT::kBytes);
   if (C == 0) return 0;
-  return ADAFLASH_FUSED_MAX_WAVES * fused_resident_clusters<DZ, DT>(C, fused_smem<DZ, DT>(rowpass_slice(vocab, C)),
-                                                                   num_sms);
+  return kFMaxWaves * fused_resident_clusters<DZ, DT>(C, fused_smem<DZ, DT>(rowpass_slice(vocab, C)), num_sms);
 }
 
 template <class DZ, class DT>

@@ -37,12 +37,10 @@ namespace adaflash {
 
 namespace {
 
-#ifndef ADAFLASH_LM_BK
-#define ADAFLASH_LM_BK 64  // hidden elements per k-block: 64 (128-byte swizzle, 2 stages) or 32 (64-byte, 4 stages)
-#endif
 constexpr int kBM = 128;  // rows per tile (TMEM lanes)
 constexpr int kBN = 256;  // vocabulary entries per tile
-constexpr int kBK = ADAFLASH_LM_BK;
+// Hidden elements per k-block: 64, one 128-byte swizzle row of bf16.
+constexpr int kBK = 64;
 constexpr int kRowBytes = kBK * 2;  // one swizzle row
 // Stage layout: A_z, A_t, then B_z and B_t, or a single B when the two heads are the
 // same matrix (one weight tile feeds both products, and the ring has room for more stages).
@@ -51,7 +49,7 @@ struct Ring {
   static constexpr uint32_t kB = kBN * kBK * 2;
   static constexpr uint32_t kA = kBM * kBK * 2;
   static constexpr uint32_t kStage = 2 * kA + (kShared ? 1 : 2) * kB;
-  static constexpr int kStages = (kBK == 32 ? 2 : 1) * (kShared ? 3 : 2);
+  static constexpr int kStages = kShared ? 3 : 2;
   static constexpr uint32_t kOffBz = 2 * kA;
   static constexpr uint32_t kOffBt = kShared ? 2 * kA : 2 * kA + kB;
 };
@@ -688,7 +686,7 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int6
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, kRowBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -56,42 +56,28 @@ namespace adaflash {
 
 namespace {
 
-// CTA shape, ring depth, stage size and resident CTAs per SM (compile-time tuning;
-// the defaults are the measured best on GB300 for bf16 logits).  The forward: two
-// CTAs per SM of 8 consumer warps, each with a 96 KB ring of three 8192-entry
-// stages of z and t.  With the gradient: four CTAs per SM of 4 consumer warps with
-// 48 KB rings of three 4096-entry stages (more CTAs per SM hide the per-row
-// exchanges better; 237 -> 228 us on a 914-row batch at V = 151936).
-#ifndef ADAFLASH_ROWPASS_CONSUMER_WARPS
-#define ADAFLASH_ROWPASS_CONSUMER_WARPS 8
-#endif
-#ifndef ADAFLASH_ROWPASS_MINBLOCKS
-#define ADAFLASH_ROWPASS_MINBLOCKS 2
-#endif
-#ifndef ADAFLASH_ROWPASS_CHUNK
-#define ADAFLASH_ROWPASS_CHUNK 8192
-#endif
-#ifndef ADAFLASH_FB_CONSUMER_WARPS
-#define ADAFLASH_FB_CONSUMER_WARPS 4
-#endif
-#ifndef ADAFLASH_FB_MINBLOCKS
-#define ADAFLASH_FB_MINBLOCKS 4
-#endif
-#ifndef ADAFLASH_FB_CHUNK
-#define ADAFLASH_FB_CHUNK 4096
-#endif
-#ifndef ADAFLASH_ROWPASS_STAGES
-#define ADAFLASH_ROWPASS_STAGES 3
-#endif
-constexpr int kStages = ADAFLASH_ROWPASS_STAGES;
+// CTA shape, ring depth, stage size and resident CTAs per SM, the measured best on
+// GB300 for bf16 logits.  The forward: two CTAs per SM of 8 consumer warps, each with
+// a 96 KB ring of three 8192-entry stages of z and t (one CTA of 16 warps, or 4096-
+// entry stages, ran slower on the 128-request batch at V = 151936).  With the
+// gradient: four CTAs per SM of 4 consumer warps with 48 KB rings of three 4096-entry
+// stages (more CTAs per SM hide the per-row exchanges better: 237 -> 228 us on a
+// 914-row batch at V = 151936; a fourth stage did not help either pass).
+constexpr int kFwdConsumerWarps = 8;
+constexpr int kFwdMinBlocks = 2;
+constexpr int kFwdChunk = 8192;
+constexpr int kGradConsumerWarps = 4;
+constexpr int kGradMinBlocks = 4;
+constexpr int kGradChunk = 4096;
+constexpr int kStages = 3;
 
 template <bool kGrad>
 struct RowCfg {
-  static constexpr int kWarps = kGrad ? ADAFLASH_FB_CONSUMER_WARPS : ADAFLASH_ROWPASS_CONSUMER_WARPS;
+  static constexpr int kWarps = kGrad ? kGradConsumerWarps : kFwdConsumerWarps;
   static constexpr int kConsumers = kWarps * 32;
   static constexpr int kThreads = kConsumers + 32;  // + one producer warp
-  static constexpr int kMinBlocks = kGrad ? ADAFLASH_FB_MINBLOCKS : ADAFLASH_ROWPASS_MINBLOCKS;
-  static constexpr int kChunk = kGrad ? ADAFLASH_FB_CHUNK : ADAFLASH_ROWPASS_CHUNK;
+  static constexpr int kMinBlocks = kGrad ? kGradMinBlocks : kFwdMinBlocks;
+  static constexpr int kChunk = kGrad ? kGradChunk : kFwdChunk;
   static_assert((kWarps & (kWarps - 1)) == 0, "a power-of-two number of consumer warps");
   static_assert((kChunk / 2) % (8 * kConsumers) == 0, "a chunk gives every consumer thread whole groups");
 };
@@ -112,16 +98,6 @@ struct StageLayout {
   static constexpr int kBytes = (kZOff + kChunk * DZ::kBytes + 16 + 127) / 128 * 128;
 };
 
-// With the gradient: L2 priority hints on the two passes' bulk copies (keep, then
-// drop), and the order of the second pass over a slice (1: last chunk first).
-#ifndef ADAFLASH_FB_L2_HINTS
-#define ADAFLASH_FB_L2_HINTS 1
-#endif
-#ifndef ADAFLASH_FB_P2_REVERSE
-#define ADAFLASH_FB_P2_REVERSE 1
-#endif
-constexpr bool kL2Hints = ADAFLASH_FB_L2_HINTS != 0;
-constexpr bool kReverseP2 = ADAFLASH_FB_P2_REVERSE != 0;
 
 }  // namespace
 
@@ -261,7 +237,9 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
         const int nch = (body + kChunk - 1) / kChunk;
         for (int pass = 0; pass < passes && !*abort_flag; ++pass) {
           for (int ci = 0; ci < nch; ++ci, ++cc) {
-            const int e0 = (pass == 1 && kReverseP2) ? (nch - 1 - ci) * kChunk : ci * kChunk;
+            // the second pass takes the slice last chunk first: those lines are the
+            // newest in L2
+            const int e0 = pass == 1 ? (nch - 1 - ci) * kChunk : ci * kChunk;
             const int st = static_cast<int>(cc % kStages);
             if (cc >= static_cast<uint32_t>(kStages) &&
                 !mbar_wait_bounded(&empty_bar[st], ((cc / kStages) & 1) ^ 1)) {
@@ -275,7 +253,8 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
             uint8_t* stage = ring + st * kStageBytes;
             const uint8_t* zsrc = U.pair ? G.zb + static_cast<int64_t>(v_begin + e0) * DZ::kBytes - zshift : nullptr;
             const uint8_t* tsrc = G.tb + static_cast<int64_t>(v_begin + e0) * DT::kBytes;
-            if (kGrad && U.pair && kL2Hints) {
+            if (kGrad && U.pair) {
+              // L2 priority: keep the first pass's lines for the second, then drop them
               const uint64_t pol = pass == 0 ? keep : drop;
               bulk_copy_g2s_hint(stage + kZOff, zsrc, bz, &full_bar[st], pol);
               bulk_copy_g2s_hint(stage, tsrc, bt, &full_bar[st], pol);
@@ -646,7 +625,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
           dispatch_shift<DZ, kShift>(G.zs2, [&](auto zs_c) {
             constexpr int ZS = decltype(zs_c)::value;
             for (int ci = 0; ci < nch; ++ci, ++cc) {
-              const int e0 = kReverseP2 ? (nch - 1 - ci) * kChunk : ci * kChunk;
+              const int e0 = (nch - 1 - ci) * kChunk;  // the producer's second-pass order
               const int st = static_cast<int>(cc % kStages);
               if (!mbar_wait_bounded(&full_bar[st], (cc / kStages) & 1)) {
                 atomicOr(&s_unit_err, 1);
@@ -738,26 +717,17 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
 // host side
 // ---------------------------------------------------------------------------
 
-#ifndef ADAFLASH_ROWPASS_TAIL
-#define ADAFLASH_ROWPASS_TAIL 1  // the last partial wave of units as a second launch with larger clusters
-#endif
-// Cluster size of a tail launch: 1 = the largest that still holds all of its rows in
-// one wave of resident CTAs, 0 = the row pass's rule (enough CTAs to fill the GPU).
-#ifndef ADAFLASH_ROWPASS_TAIL_ONE_WAVE
-#define ADAFLASH_ROWPASS_TAIL_ONE_WAVE 1
-#endif
-constexpr bool kTailOneWave = ADAFLASH_ROWPASS_TAIL_ONE_WAVE != 0;
-#ifndef ADAFLASH_ROWPASS_SLICE_TARGET
-#define ADAFLASH_ROWPASS_SLICE_TARGET 160000
-#endif
+// Entries of a row per CTA of the forward row pass, at most (V = 151936 gives one
+// CTA per row when the batch fills the GPU).
+constexpr int kSliceTarget = 160000;
 
 int rowpass_cluster_size(int vocab, int units, int num_sms) {
-  // At most ADAFLASH_ROWPASS_SLICE_TARGET entries per CTA, and enough CTAs in
+  // At most kSliceTarget entries per CTA, and enough CTAs in
   // flight to fill the GPU (the resident CTAs per SM) when there are few rows; at most 8 (the
   // portable cluster size).
-  int c = (vocab + ADAFLASH_ROWPASS_SLICE_TARGET - 1) / ADAFLASH_ROWPASS_SLICE_TARGET;
+  int c = (vocab + kSliceTarget - 1) / kSliceTarget;
   if (c < 1) c = 1;
-  while (c < kMaxCluster && static_cast<long long>(units) * c < static_cast<long long>(ADAFLASH_ROWPASS_MINBLOCKS) * num_sms) ++c;
+  while (c < kMaxCluster && static_cast<long long>(units) * c < static_cast<long long>(kFwdMinBlocks) * num_sms) ++c;
   return c > kMaxCluster ? kMaxCluster : c;
 }
 
@@ -886,7 +856,7 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   const int split = (units / clusters) * clusters;
   // With the gradient, a last partial wave of target-only rows (cheap: no second pass)
   // stays in the one launch rather than costing a launch of its own.
-  if (!ADAFLASH_ROWPASS_TAIL || units <= clusters || split == units || p.cluster >= kMaxCluster ||
+  if (units <= clusters || split == units || p.cluster >= kMaxCluster ||
       (kGrad && p0.mode == kModeFwd && split >= p0.N_d))
     return launch_range<DZ, DT, kGrad, kShift>(p, true, stream);
   const RowPassParams base = p;
@@ -898,15 +868,13 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
     tail.unit_begin = b;
     tail.unit_end = end;
     tail.wait_prior = 1;
-    if (kTailOneWave) {
-      // the largest cluster that still fits all of the tail's rows in one wave
-      const long long cap = static_cast<long long>(RowCfg<kGrad>::kMinBlocks) * sm_count();
-      int c = 1;
-      while (c < kMaxCluster && static_cast<long long>(end - b) * (c + 1) <= cap) ++c;
-      tail.cluster = c;
-    } else {
-      tail.cluster = rowpass_cluster_size(p.V, end - b, sm_count());
-    }
+    // the largest cluster that still fits all of the tail's rows in one wave (filling
+    // the GPU instead took a second partial wave: 110.4 against 106.7 us for the
+    // forward on a 128-request batch at V = 151936)
+    const long long cap = static_cast<long long>(RowCfg<kGrad>::kMinBlocks) * sm_count();
+    int c = 1;
+    while (c < kMaxCluster && static_cast<long long>(end - b) * (c + 1) <= cap) ++c;
+    tail.cluster = c;
     if (tail.cluster < p.cluster) tail.cluster = p.cluster;
     tail.slice = rowpass_slice(p.V, tail.cluster);
     return launch_range<DZ, DT, kGrad, kShift>(tail, true, stream);

@@ -30,25 +30,15 @@ namespace adaflash {
 
 namespace {
 
-#ifndef ADAFLASH_LSE_THREADS
-#define ADAFLASH_LSE_THREADS 256
-#endif
-#ifndef ADAFLASH_LSE_UNROLL
-#define ADAFLASH_LSE_UNROLL 8
-#endif
-#ifndef ADAFLASH_LSE_MINBLOCKS
-#define ADAFLASH_LSE_MINBLOCKS 4  // resident S1 CTAs per SM the register budget must allow
-#endif
-#ifndef ADAFLASH_LSE_ROWS_PER_SM
-#define ADAFLASH_LSE_ROWS_PER_SM 12  // S1 splits rows over a cluster until there are this many units per SM
-#endif
-
-#ifndef ADAFLASH_DRAW_MINBLOCKS
-#define ADAFLASH_DRAW_MINBLOCKS 8  // resident S2 CTAs per SM: 8 CTAs x 152 SMs hold 128+ requests at once
-#endif
-
-constexpr int kLseThreads = ADAFLASH_LSE_THREADS;
-constexpr int kLseUnroll = ADAFLASH_LSE_UNROLL;  // 16-byte loads in flight per thread
+// S1: 256-thread CTAs with eight 16-byte loads in flight per thread, four resident
+// CTAs per SM; a row is split over a cluster of up to 8 CTAs while there are fewer
+// than 12 row units per SM.  S2: 256-thread CTAs, eight resident per SM, so that
+// 8 x 152 CTAs hold every request of a 128-request batch at once.
+constexpr int kLseThreads = 256;
+constexpr int kLseUnroll = 8;  // 16-byte loads in flight per thread
+constexpr int kLseMinBlocks = 4;
+constexpr int kLseRowsPerSm = 12;
+constexpr int kDrawMinBlocks = 8;
 constexpr int kLseMaxCluster = 8;
 constexpr int kDrawThreads = 256;  // per CTA
 constexpr int kDrawCluster = 8;    // CTAs per request
@@ -251,7 +241,7 @@ __device__ __forceinline__ bool is_aligned16(const void* p) {
 
 // ---- S1: log-sum-exp at temperature of every draft row and every target row ----
 template <class DZ, class DT>
-__global__ void __launch_bounds__(kLseThreads, ADAFLASH_LSE_MINBLOCKS) lse_rows_kernel(const SampledParams P, int C) {
+__global__ void __launch_bounds__(kLseThreads, kLseMinBlocks) lse_rows_kernel(const SampledParams P, int C) {
   __shared__ float red[64];
   __shared__ float part[2 * kLseMaxCluster];
   // S1 is a programmatic dependent of whatever the stream ran before it: nothing in
@@ -295,7 +285,7 @@ __global__ void __launch_bounds__(kLseThreads, ADAFLASH_LSE_MINBLOCKS) lse_rows_
 // sums give, in vocabulary order, each warp's prefix; the owner warp stages its
 // segment's weights in shared memory and walks it tile by tile.
 template <class DZ, class DT>
-__global__ void __launch_bounds__(kDrawThreads, ADAFLASH_DRAW_MINBLOCKS) sampled_draw_kernel(const SampledParams P,
+__global__ void __launch_bounds__(kDrawThreads, kDrawMinBlocks) sampled_draw_kernel(const SampledParams P,
                                                                                               int seg_tiles) {
   extern __shared__ float wbuf[];  // seg_tiles * 256 weights of the owner warp's segment
   __shared__ float scan[kDrawThreads / 32];
@@ -566,7 +556,7 @@ __global__ void __launch_bounds__(kDrawThreads, ADAFLASH_DRAW_MINBLOCKS) sampled
 static int lse_cluster_size(int rows, int num_sms) {
   int C = 1;
   while (C < kLseMaxCluster &&
-         static_cast<int64_t>(rows) * C < static_cast<int64_t>(ADAFLASH_LSE_ROWS_PER_SM) * num_sms)
+         static_cast<int64_t>(rows) * C < static_cast<int64_t>(kLseRowsPerSm) * num_sms)
     C *= 2;
   return C;
 }
