@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
         rc.bgrp = all.bgrp;
         rc.mt = all.mt;
         rc.argmax = (rank == 0 && !U.bad && !(kGrad && U.pair))
-                        ? resolve_argmax_grid<DT>(trow, all.bgrp, all.mt, P.V, G.H)
+                        ? resolve_argmax_grid<DZ, DT>(trow, zrow, all.bgrp, all.mt, P.V, G.H, &rc.za)
                         : -1;
         rc.err = all.err | werr;
         rc.stop = *abort_flag;
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
           const int a = rc.argmax;
           const int64_t d = U.d;
           P.kl_row[d] = rc.kl_unclip - corr_all;
-          P.ce_row[d] = rc.lse_z - DZ::load(zrow, a);
+          P.ce_row[d] = rc.lse_z - rc.za;
           P.row_stats[4 * d + 0] = rc.lse_z;
           P.row_stats[4 * d + 1] = rc.lse_t;
           P.row_stats[4 * d + 2] = (rc.kl_unclip + 1.f) - sclip_all;

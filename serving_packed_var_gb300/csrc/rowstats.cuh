@@ -45,6 +45,7 @@ struct RowConsts {
   float lse_z, lse_t, dlse, kl_unclip;
   float theta;
   int argmax;
+  float za;  // the draft logit at argmax (pair rows of the forward)
   int bgrp;  // first (row-global) group holding the max of t
   float mt;  // the max of t
   int err;
@@ -372,9 +373,13 @@ namespace {
 
 // Lowest index of the value mt inside row-global group grp of a target row whose
 // groups follow its 16-byte grid: group 0 is the head [0, H) and group G >= 1 holds
-// entries [H + 8 (G - 1), H + 8 G) (-1 if absent or out of range).
-template <class DT>
-__device__ int resolve_argmax_grid(const uint8_t* trow, int grp, float mt, int V, int H) {
+// entries [H + 8 (G - 1), H + 8 G) (-1 if absent or out of range).  With a draft row,
+// *za receives the draft logit at that index.  Every entry of the group (and of the
+// draft row's group) is loaded before the search, so the re-read costs one round trip
+// to memory rather than one per entry.
+template <class DZ, class DT>
+__device__ int resolve_argmax_grid(const uint8_t* trow, const uint8_t* zrow, int grp, float mt, int V, int H,
+                                   float* za) {
   if (grp < 0) return -1;
   int v0, n;
   if (grp == 0) {
@@ -386,9 +391,24 @@ __device__ int resolve_argmax_grid(const uint8_t* trow, int grp, float mt, int V
     v0 = static_cast<int>(s);
     n = min(8, V - v0);
   }
-  for (int j = 0; j < n; ++j)
-    if (DT::load(trow, v0 + j) == mt) return v0 + j;
-  return -1;
+  const float nan = __int_as_float(0x7fc00000);  // equal to nothing
+  float t[8], z[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    t[j] = j < n ? DT::load(trow, v0 + j) : nan;
+    z[j] = (zrow != nullptr && j < n) ? DZ::load(zrow, v0 + j) : 0.f;
+  }
+  int a = -1;
+  float zv = 0.f;
+#pragma unroll
+  for (int j = 7; j >= 0; --j) {
+    if (t[j] == mt) {
+      a = v0 + j;
+      zv = z[j];
+    }
+  }
+  if (za != nullptr) *za = zv;
+  return a;
 }
 
 }  // namespace

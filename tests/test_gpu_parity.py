@@ -146,6 +146,9 @@ EDGE = [
     dict(vocab=4096, k=[16] * 40, accept="uniform"),
     dict(vocab=2048, k=[6, 2], ld_d=2048 + 5, ld_t=2048 + 3),
     dict(vocab=3000, k=[9], clip_c=0.01),
+    # the largest vocabulary the library takes, on and off the 16-byte grid
+    dict(vocab=524288, k=[16, 1], d_dtype="fp32", t_dtype="fp32"),
+    dict(vocab=524287, k=[5, 2], d_dtype="fp32", t_dtype="bf16"),
 ]
 
 

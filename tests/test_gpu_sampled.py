@@ -226,6 +226,8 @@ EDGE = [
     dict(vocab=4097, k=[2, 7, 1], d_dtype="bf16", t_dtype="fp32"),
     dict(vocab=2048, k=[6, 2], ld_d=2048 + 5, ld_t=2048 + 3),
     dict(vocab=96, k=list(np.random.default_rng(9).integers(1, 17, size=300)), d_dtype="fp32", t_dtype="fp32"),
+    dict(vocab=524288, k=[16, 1], d_dtype="bf16", t_dtype="bf16"),
+    dict(vocab=524287, k=[4, 9], d_dtype="fp32", t_dtype="bf16"),
 ]
 
 
