@@ -1,0 +1,83 @@
+"""A host model of how the row pass cuts one row into groups, slices, chunks and direct loads.
+
+The row pass (K1 / K1g) follows each target row's own 16-byte grid: the first H entries (the
+head, before the row's first 16-byte boundary, H < 16 / element bytes) form group 0, read by
+rank 0 with element loads; the body [H, V) is cut into 8-entry groups 1, 2, ... and into the
+cluster's C slices of `slice` entries (a multiple of 8).  Inside a slice, whole chunks of 8-entry
+groups go through the bulk-copy ring; what is left of the slice (fewer than 8 entries at its end)
+and the head are direct loads, group g going to consumer thread g mod (consumer threads).
+
+The model restates that arithmetic and checks, for every vocabulary size, cluster size, head
+length and CTA shape listed, that every entry of the row is visited exactly once and that the
+group it is visited in is the group the argmax re-read searches for it.  A plausible slip in
+the kernel's index arithmetic (a slice boundary off by one group, the head counted twice, a
+ragged end skipped) fails one of these cases.  It checks the partition, not the kernel: the GPU
+parity tests check the kernel's outputs.
+"""
+
+import pytest
+
+
+def slice_entries(V, C):
+    per = (V + C - 1) // C
+    return (per + 7) & ~7
+
+
+def visit_row(V, C, head_offset_bytes, elem_bytes, chunk, consumers):
+    H = min(((16 - head_offset_bytes % 16) % 16) // elem_bytes, V)
+    Vb = V - H
+    S = slice_entries(V, C)
+    seen = {}
+    for rank in range(C):
+        vb = rank * S
+        ve = min(Vb, vb + S)
+        length = max(0, ve - vb)
+        ngroups = (length + 7) >> 3
+        body = length & ~7
+        has_head = 1 if (rank == 0 and H > 0) else 0
+        ngx = ngroups + has_head
+        gfirst = 1 + (vb >> 3)
+        for e0 in range(0, body, chunk):  # the ring's chunks
+            for g in range(min(chunk, body - e0) >> 3):
+                grp = gfirst + (e0 >> 3) + g
+                for j in range(8):
+                    seen.setdefault(H + vb + e0 + 8 * g + j, []).append(grp)
+        for tid in range(consumers):  # direct loads: the ragged end, and the head on rank 0
+            g = (body >> 3) + ((tid - (body >> 3)) & (consumers - 1))
+            while g < ngx:
+                head = g == ngroups
+                v0 = 0 if head else H + vb + (g << 3)
+                n = H if head else min(8, ve - (vb + (g << 3)))
+                grp = 0 if head else gfirst + g
+                for j in range(n):
+                    seen.setdefault(v0 + j, []).append(grp)
+                g += consumers
+    assert sorted(seen) == list(range(V)), ("entries", V, C, head_offset_bytes, elem_bytes)
+    for v, groups in seen.items():
+        assert len(groups) == 1, ("visited twice", v)
+        grp = groups[0]
+        lo, n = (0, H) if grp == 0 else (H + 8 * (grp - 1), min(8, V - (H + 8 * (grp - 1))))
+        assert lo <= v < lo + n, ("argmax re-read misses", v, grp)
+
+
+# (entries per chunk, consumer threads): the forward for two 16-bit inputs, the pass with
+# the gradient, and either one with a float32 input (half the entries per chunk)
+SHAPES = [(8192, 256), (4096, 128), (4096, 256), (2048, 128)]
+
+
+@pytest.mark.parametrize("elem_bytes", [2, 4])
+def test_small_rows_every_cluster_and_head(elem_bytes):
+    for V in range(1, 40):
+        for C in range(1, 9):
+            for off in range(0, 16, elem_bytes):
+                for chunk, consumers in SHAPES:
+                    visit_row(V, C, off, elem_bytes, chunk, consumers)
+
+
+@pytest.mark.parametrize("V", [1001, 4097, 8200, 151936, 151937])
+def test_large_rows(V):
+    for C in (1, 2, 6, 8):
+        for elem_bytes, offs in ((2, (0, 2, 14)), (4, (0, 4, 12))):
+            for off in offs:
+                for chunk, consumers in SHAPES[:2]:
+                    visit_row(V, C, off, elem_bytes, chunk, consumers)
