@@ -20,8 +20,15 @@
  * at element r*ld; columns ld > vocab are never read.  Element types: float32 or
  * bfloat16 (ADAFLASH_FP32 / ADAFLASH_BF16); supported (draft, target) pairs are
  * (fp32, fp32), (bf16, bf16), (fp32, bf16) and (bf16, fp32).  Any element-aligned
- * base pointer and any ld >= vocab are accepted; rows whose start is 16-byte
- * aligned take the bulk-copy path, others a slower direct-load path.
+ * base pointer and any ld >= vocab are accepted.  Every row is bulk-copied: the
+ * entries before a target row's first 16-byte boundary (under 16 bytes of them) are
+ * read one by one, and a draft row that is off that grid is copied from the 16-byte
+ * boundary just below it.
+ *
+ * Empty batch: num_requests = num_draft_rows = 0 is valid.  Nothing is read and no
+ * kernel is launched, so the row, token, offset and per-row output pointers may be
+ * NULL; the scalar arguments are still checked, and an entry point with a loss
+ * output sets *loss = 0 (its loss pointer must be valid).
  *
  * Ownership and ordering: every pointer argument of the GPU entry points is a
  * DEVICE pointer owned by the caller.  They allocate nothing, keep no state between

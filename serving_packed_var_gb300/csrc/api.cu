@@ -95,6 +95,17 @@ long long l2_bytes() {
     if ((expr) != cudaSuccess) return ADAFLASH_ERR_CUDA; \
   } while (0)
 
+// An empty batch (no requests, so no rows): nothing is read, whatever the row and
+// token pointers hold (NULL included); the only write is loss = 0 where the entry
+// point has a loss.
+adaflash_status empty_batch(float* loss, bool has_loss, const uint32_t* d_status, cudaStream_t s) {
+  if (has_loss && !int_ptr_ok(loss)) return ADAFLASH_ERR_INVALID_ARG;
+  if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
+  ADAFLASH_TRY(check_device());
+  if (has_loss) ADAFLASH_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
+  return ADAFLASH_OK;
+}
+
 }  // namespace
 
 namespace adaflash {
@@ -125,14 +136,14 @@ adaflash_status adaflash_verify_packed(const void* target_logits, adaflash_dtype
                                        int32_t* target_argmax, int32_t* accept_len, int32_t* bonus_token,
                                        float* accept_rate, uint32_t* d_status, void* stream) {
   ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_requests == 0) return empty_batch(nullptr, false, d_status, s);
   ADAFLASH_TRY(check_logits(target_logits, t_dtype, ld_t, vocab));
   if (!int_ptr_ok(draft_tokens) || !int_ptr_ok(draft_offsets) || !int_ptr_ok(target_argmax) ||
       !int_ptr_ok(accept_len) || !int_ptr_ok(bonus_token) || !int_ptr_ok(accept_rate))
     return ADAFLASH_ERR_INVALID_ARG;
   if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
   ADAFLASH_TRY(check_device());
-  if (num_requests == 0) return ADAFLASH_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   RowPassParams p = {};
   p.t = target_logits;
@@ -174,6 +185,9 @@ adaflash_status adaflash_opd_loss_fwd(const void* draft_logits, adaflash_dtype d
                                       int32_t* bonus_token, float* accept_rate, float* kl_row, float* ce_row,
                                       float* row_stats, float* loss, uint32_t* d_status, void* stream) {
   ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight)) return ADAFLASH_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_requests == 0) return empty_batch(loss, true, d_status, s);
   ADAFLASH_TRY(check_logits(draft_logits, d_dtype, ld_d, vocab));
   ADAFLASH_TRY(check_logits(target_logits, t_dtype, ld_t, vocab));
   if (!int_ptr_ok(draft_tokens) || !int_ptr_ok(draft_offsets) || !int_ptr_ok(target_argmax) ||
@@ -181,13 +195,7 @@ adaflash_status adaflash_opd_loss_fwd(const void* draft_logits, adaflash_dtype d
       !int_ptr_ok(ce_row) || !int_ptr_ok(row_stats) || !int_ptr_ok(loss))
     return ADAFLASH_ERR_INVALID_ARG;
   if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
-  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight)) return ADAFLASH_ERR_INVALID_ARG;
   ADAFLASH_TRY(check_device());
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (num_requests == 0) {
-    ADAFLASH_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
-    return ADAFLASH_OK;
-  }
 
   RowPassParams p = {};
   p.z = draft_logits;
@@ -238,6 +246,9 @@ adaflash_status adaflash_opd_loss_bwd(const void* draft_logits, adaflash_dtype d
                                       const float* row_stats, const float* grad_row, float grad_scale,
                                       float* grad_draft, int64_t ld_g, uint32_t* d_status, void* stream) {
   ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight) || !std::isfinite(grad_scale)) return ADAFLASH_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_requests == 0) return empty_batch(nullptr, false, d_status, s);
   ADAFLASH_TRY(check_logits(draft_logits, d_dtype, ld_d, vocab));
   ADAFLASH_TRY(check_logits(target_logits, t_dtype, ld_t, vocab));
   if (!int_ptr_ok(draft_offsets) || !int_ptr_ok(target_argmax) || !int_ptr_ok(row_stats) ||
@@ -245,10 +256,7 @@ adaflash_status adaflash_opd_loss_bwd(const void* draft_logits, adaflash_dtype d
     return ADAFLASH_ERR_INVALID_ARG;
   if (grad_row && !aligned(grad_row, 4)) return ADAFLASH_ERR_INVALID_ARG;
   if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
-  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight) || !std::isfinite(grad_scale)) return ADAFLASH_ERR_INVALID_ARG;
   ADAFLASH_TRY(check_device());
-  if (num_requests == 0) return ADAFLASH_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   BwdParams p = {};
   p.z = draft_logits;
@@ -286,6 +294,9 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
                                           float* loss, float* grad_draft, int64_t ld_g, uint32_t* d_status,
                                           void* stream) {
   ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight) || !std::isfinite(grad_scale)) return ADAFLASH_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_requests == 0) return empty_batch(loss, true, d_status, s);
   ADAFLASH_TRY(check_logits(draft_logits, d_dtype, ld_d, vocab));
   ADAFLASH_TRY(check_logits(target_logits, t_dtype, ld_t, vocab));
   if (!int_ptr_ok(draft_tokens) || !int_ptr_ok(draft_offsets) || !int_ptr_ok(target_argmax) ||
@@ -294,13 +305,7 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
     return ADAFLASH_ERR_INVALID_ARG;
   if (grad_row && !aligned(grad_row, 4)) return ADAFLASH_ERR_INVALID_ARG;
   if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
-  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight) || !std::isfinite(grad_scale)) return ADAFLASH_ERR_INVALID_ARG;
   ADAFLASH_TRY(check_device());
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (num_requests == 0) {
-    ADAFLASH_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
-    return ADAFLASH_OK;
-  }
 
   RowPassParams p = {};
   p.z = draft_logits;
@@ -429,6 +434,9 @@ adaflash_status check_lmhead_fwd_args(const void* draft_hidden, int64_t ld_hd, c
                                       float* ce_row, float* row_stats, float* loss, uint32_t* d_status) {
   ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
   if (hidden < 64 || hidden % 64 != 0) return ADAFLASH_ERR_INVALID_ARG;
+  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight)) return ADAFLASH_ERR_INVALID_ARG;
+  if (num_requests == 0)  // an empty batch reads nothing: only the loss pointer matters
+    return int_ptr_ok(loss) && (!d_status || aligned(d_status, 4)) ? ADAFLASH_OK : ADAFLASH_ERR_INVALID_ARG;
   ADAFLASH_TRY(check_bf16_rows(draft_hidden, ld_hd, hidden));
   ADAFLASH_TRY(check_bf16_rows(target_hidden, ld_ht, hidden));
   ADAFLASH_TRY(check_bf16_rows(draft_head, ld_wd, hidden));
@@ -438,7 +446,6 @@ adaflash_status check_lmhead_fwd_args(const void* draft_hidden, int64_t ld_hd, c
       !int_ptr_ok(ce_row) || !int_ptr_ok(row_stats) || !int_ptr_ok(loss))
     return ADAFLASH_ERR_INVALID_ARG;
   if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
-  if (!(clip_c > 0.0f) || !std::isfinite(ce_weight)) return ADAFLASH_ERR_INVALID_ARG;
   return ADAFLASH_OK;
 }
 }  // namespace
@@ -457,14 +464,11 @@ adaflash_status adaflash_lmhead_opd_fwd(const void* draft_hidden, int64_t ld_hd,
                                      hidden, draft_tokens, draft_offsets, num_requests, num_draft_rows, vocab, clip_c,
                                      ce_weight, target_argmax, accept_len, bonus_token, accept_rate, kl_row, ce_row,
                                      row_stats, loss, d_status));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_requests == 0) return empty_batch(loss, true, d_status, s);
   const int64_t need = adaflash_lmhead_workspace_bytes(num_requests, num_draft_rows, vocab, hidden);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return ADAFLASH_ERR_INVALID_ARG;
   ADAFLASH_TRY(check_device());
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (num_requests == 0) {
-    ADAFLASH_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
-    return ADAFLASH_OK;
-  }
   const int32_t Nt = num_draft_rows + num_requests;
   uint16_t* ht_pairs = static_cast<uint16_t*>(workspace);
   LmPartial* partials =
@@ -540,6 +544,7 @@ adaflash_status adaflash_lmhead_opd_fwd_static(const void* draft_hidden, int64_t
                                      hidden, draft_tokens, draft_offsets, num_requests, num_draft_rows, vocab, clip_c,
                                      ce_weight, target_argmax, accept_len, bonus_token, accept_rate, kl_row, ce_row,
                                      row_stats, loss, d_status));
+  if (num_requests == 0) return empty_batch(loss, true, d_status, static_cast<cudaStream_t>(stream));
   const int64_t need = adaflash_lmhead_workspace_bytes(num_requests, num_draft_rows, vocab, hidden);
   if (need < 0) return ADAFLASH_ERR_INVALID_ARG;
   if (need > ADAFLASH_LMHEAD_STATIC_SCRATCH_BYTES) return ADAFLASH_ERR_UNSUPPORTED;
@@ -561,6 +566,9 @@ adaflash_status adaflash_verify_sampled(const void* draft_logits, adaflash_dtype
                                         float* row_lse, int32_t* accept_len, int32_t* next_token,
                                         float* accept_rate, uint32_t* d_status, void* stream) {
   ADAFLASH_TRY(check_shape(num_requests, num_draft_rows, vocab));
+  if (!(temperature > 0.0f) || !std::isfinite(temperature) || !std::isfinite(1.0f / temperature))
+    return ADAFLASH_ERR_INVALID_ARG;
+  if (num_requests == 0) return empty_batch(nullptr, false, d_status, static_cast<cudaStream_t>(stream));
   ADAFLASH_TRY(check_logits(draft_logits, d_dtype, ld_d, vocab));
   ADAFLASH_TRY(check_logits(target_logits, t_dtype, ld_t, vocab));
   if (!int_ptr_ok(draft_tokens) || !int_ptr_ok(draft_offsets) || !int_ptr_ok(u_accept) ||
@@ -568,10 +576,7 @@ adaflash_status adaflash_verify_sampled(const void* draft_logits, adaflash_dtype
       !int_ptr_ok(accept_rate))
     return ADAFLASH_ERR_INVALID_ARG;
   if (d_status && !aligned(d_status, 4)) return ADAFLASH_ERR_INVALID_ARG;
-  if (!(temperature > 0.0f) || !std::isfinite(temperature) || !std::isfinite(1.0f / temperature))
-    return ADAFLASH_ERR_INVALID_ARG;
   ADAFLASH_TRY(check_device());
-  if (num_requests == 0) return ADAFLASH_OK;
 
   SampledParams p = {};
   p.z = draft_logits;

@@ -70,6 +70,20 @@ def test_verify_rejects(lib, kw):
     assert _verify(lib, **kw) == INVALID
 
 
+def test_empty_batch_reads_no_row_pointers(lib):
+    # An empty batch passes the argument checks with NULL row, token, offset and output
+    # pointers: the status is the device check's (OK on a GB300), never INVALID_ARG.  No
+    # case here reaches a write (the loss write of an empty forward is not exercised).
+    empty = dict(R=0, Nd=0)
+    assert _verify(lib, t=None, tok=None, doff=None, amax=None, acc=None, bonus=None, rate=None, **empty) != INVALID
+    assert _bwd(lib, z=None, t=None, doff=None, amax=None, stats=None, g=None, **empty) != INVALID
+    # what is still checked: the loss pointer, the scalars, the counts
+    assert _fwd(lib, z=None, t=None, tok=None, doff=None, loss=None, **empty) == INVALID
+    assert _fwd(lib, c=0.0, loss=None, **empty) == INVALID
+    assert _bwd(lib, gs=float("nan"), **empty) == INVALID
+    assert _verify(lib, R=0, Nd=3) == INVALID
+
+
 def test_verify_vocab_too_large(lib):
     V = _native.ADAFLASH_MAX_VOCAB + 1
     assert _verify(lib, V=V, ld_t=V) == UNSUPPORTED
