@@ -342,8 +342,12 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
     ADAFLASH_CUDA(launch_fused(p, d_dtype, t_dtype, num_sms(), s));
   } else {
     const int row_bytes = vocab * (dtype_bytes(d_dtype) + dtype_bytes(t_dtype));
-    p.cluster = rowpass_grad_cluster_size(vocab, p.N_d + p.R, row_bytes, rowpass_grad_chunk(d_dtype, t_dtype),
-                                          num_sms(), l2_bytes());
+    int c = 0;
+    if (static_cast<long long>(p.N_d) * row_bytes <= l2_bytes() * 3 / 4)
+      c = rowpass_grad_one_round_cluster(d_dtype, t_dtype, aligned16, vocab, p.N_d);
+    p.cluster = c > 0 ? c
+                      : rowpass_grad_cluster_size(vocab, p.N_d + p.R, row_bytes, rowpass_grad_chunk(d_dtype, t_dtype),
+                                                  num_sms(), l2_bytes());
     p.slice = rowpass_slice(vocab, p.cluster);
     ADAFLASH_CUDA(launch_rowpass_grad(p, d_dtype, t_dtype, aligned16, s));
   }

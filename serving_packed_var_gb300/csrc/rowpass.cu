@@ -927,6 +927,36 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   return launch_tail(split, units);
 }
 
+// With every paired row of the batch in L2 at once, the largest cluster size whose
+// resident clusters take all paired rows in one round: more CTAs per row shorten each
+// row, and no partly empty second round of paired rows follows (the bonus rows, a
+// quarter of a paired row's work each, may spill over).  Measured on GB300, k = 16 per
+// request at V = 151936, bf16 (us per call, the general rule's C = 6 in brackets): 3
+// requests C = 8 19.8 (23.7); 4 requests C = 8 23.7 (23.8); 6 requests C = 6 31.1 (the
+// same); 8 requests C = 4 40.1 (50.3).  0 when no size from 2 to 8 takes them.
+template <class DZ, class DT, bool kShift>
+static int one_round_cluster_t(int vocab, int pairs) {
+  for (int c = kMaxCluster; c >= 2; --c) {
+    const size_t smem = rowpass_smem<DZ, DT, true>(rowpass_slice(vocab, c));
+    if (active_clusters<DZ, DT, true, kShift>(c, smem) >= pairs) return c;
+  }
+  return 0;
+}
+
+template <bool kShift>
+static int one_round_cluster_dtypes(int z_dtype, int t_dtype, int vocab, int pairs) {
+  const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
+  if (zb && tb) return one_round_cluster_t<BF16, BF16, kShift>(vocab, pairs);
+  if (!zb && tb) return one_round_cluster_t<F32, BF16, kShift>(vocab, pairs);
+  if (zb && !tb) return one_round_cluster_t<BF16, F32, kShift>(vocab, pairs);
+  return one_round_cluster_t<F32, F32, kShift>(vocab, pairs);
+}
+
+int rowpass_grad_one_round_cluster(int z_dtype, int t_dtype, bool aligned, int vocab, int pairs) {
+  return aligned ? one_round_cluster_dtypes<false>(z_dtype, t_dtype, vocab, pairs)
+                 : one_round_cluster_dtypes<true>(z_dtype, t_dtype, vocab, pairs);
+}
+
 int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int chunk_entries, int num_sms, long long l2_bytes) {
   // The row pass's size, then at least 6 CTAs while each CTA's slice still holds four
   // ring chunks (C = 6 measured best on GB300 for bf16 rows and for fp32-draft /
