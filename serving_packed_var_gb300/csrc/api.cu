@@ -154,13 +154,15 @@ adaflash_status adaflash_verify_packed(const void* target_logits, adaflash_dtype
   p.N_t = num_draft_rows + num_requests;
   p.V = vocab;
   p.mode = kModeVerify;
-  p.cluster = rowpass_cluster_size(vocab, p.mode == kModeVerify ? p.N_t : p.N_d + p.R, num_sms());
+  // Target-only units read no draft row; the draft dtype only sizes the ring.
+  const bool aligned = rows_16b(target_logits, ld_t, dtype_bytes(t_dtype));
+  const int c = rowpass_one_round_cluster(1, t_dtype, aligned, vocab, p.N_t);
+  p.cluster = c > 0 ? c : rowpass_cluster_size(vocab, p.N_t, num_sms());
   p.slice = rowpass_slice(vocab, p.cluster);
   p.clip_c = 1.0f;
   p.target_argmax = target_argmax;
   p.status = d_status;
-  // Target-only units read no draft row; the draft dtype only sizes the ring.
-  ADAFLASH_CUDA(launch_rowpass(p, 1, t_dtype, rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)), s));
+  ADAFLASH_CUDA(launch_rowpass(p, 1, t_dtype, aligned, s));
 
   FinalizeParams f = {};
   f.tokens = draft_tokens;
@@ -208,7 +210,12 @@ adaflash_status adaflash_opd_loss_fwd(const void* draft_logits, adaflash_dtype d
   p.N_t = num_draft_rows + num_requests;
   p.V = vocab;
   p.mode = kModeFwd;
-  p.cluster = rowpass_cluster_size(vocab, p.mode == kModeVerify ? p.N_t : p.N_d + p.R, num_sms());
+  const bool aligned = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
+                       rows_16b(target_logits, ld_t, dtype_bytes(t_dtype));
+  // all row units in one round of resident clusters where a cluster size allows it,
+  // else enough CTAs to fill the GPU
+  const int c = rowpass_one_round_cluster(d_dtype, t_dtype, aligned, vocab, p.N_d + p.R);
+  p.cluster = c > 0 ? c : rowpass_cluster_size(vocab, p.N_d + p.R, num_sms());
   p.slice = rowpass_slice(vocab, p.cluster);
   p.clip_c = clip_c;
   p.target_argmax = target_argmax;
@@ -216,8 +223,6 @@ adaflash_status adaflash_opd_loss_fwd(const void* draft_logits, adaflash_dtype d
   p.ce_row = ce_row;
   p.row_stats = row_stats;
   p.status = d_status;
-  const bool aligned = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
-                       rows_16b(target_logits, ld_t, dtype_bytes(t_dtype));
   ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype, aligned, s));
 
   FinalizeParams f = {};

@@ -137,8 +137,10 @@ cudaError_t launch_rowpass(const RowPassParams& p, int z_dtype, int t_dtype, boo
 // rows).  Cluster size: rowpass_grad_cluster_size (row_bytes = V (b_z + b_t)).
 cudaError_t launch_rowpass_grad(const RowPassParams& p, int z_dtype, int t_dtype, bool aligned, cudaStream_t s);
 int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int chunk_entries, int num_sms, long long l2_bytes);
-// For batches whose paired rows all fit the L2 at once: the largest cluster size that
-// takes every paired row in one round of resident clusters, else 0.
+// The largest cluster size that takes every row unit in one round of resident clusters
+// (else 0): for the forward and verification (units: their rows), and for the pass with
+// the gradient on batches whose paired rows all fit the L2 at once (pairs: paired rows).
+int rowpass_one_round_cluster(int z_dtype, int t_dtype, bool aligned, int vocab, int units);
 int rowpass_grad_one_round_cluster(int z_dtype, int t_dtype, bool aligned, int vocab, int pairs);
 int rowpass_grad_chunk(int z_dtype, int t_dtype);  // vocabulary entries per ring stage
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);

@@ -927,34 +927,46 @@ static cudaError_t launch_one(const RowPassParams& p0, cudaStream_t stream) {
   return launch_tail(split, units);
 }
 
-// With every paired row of the batch in L2 at once, the largest cluster size whose
-// resident clusters take all paired rows in one round: more CTAs per row shorten each
-// row, and no partly empty second round of paired rows follows (the bonus rows, a
-// quarter of a paired row's work each, may spill over).  Measured on GB300, k = 16 per
-// request at V = 151936, bf16 (us per call, the general rule's C = 6 in brackets): 3
-// requests C = 8 19.8 (23.7); 4 requests C = 8 23.7 (23.8); 6 requests C = 6 31.1 (the
-// same); 8 requests C = 4 40.1 (50.3).  0 when no size from 2 to 8 takes them.
-template <class DZ, class DT, bool kShift>
-static int one_round_cluster_t(int vocab, int pairs) {
-  for (int c = kMaxCluster; c >= 2; --c) {
-    const size_t smem = rowpass_smem<DZ, DT, true>(rowpass_slice(vocab, c));
-    if (active_clusters<DZ, DT, true, kShift>(c, smem) >= pairs) return c;
+// The largest cluster size (from 8 down to 1, or to 2 with the gradient) whose resident
+// clusters take `units` row units in one round: more CTAs per row shorten each row, and
+// no partly empty second round follows; 0 when no size does.
+//
+// The forward and verification use it for any batch (the units are its rows): measured
+// on GB300, k = 16 per request at V = 151936, bf16, forward / verification us per call
+// (the fill-the-GPU rule of rowpass_cluster_size in brackets): 3 requests C = 5 15.5 /
+// 13.1 (18.1 / 15.0); 4 requests C = 4 16.0 / 14.1 (19.1 / 15.4); 8 requests C = 2 20.6
+// / 12.8 (25.7 / 15.5); 16 requests C = 1 35.4 / 13.9 (41.4 / 17.9).
+//
+// The pass with the gradient uses it, counting paired rows only (the bonus rows, a
+// quarter of a paired row's work each, may spill over), when every paired row fits the
+// L2 budget at once: 3 requests C = 8 19.6 us (23.5 with the general rule's C = 6);
+// 8 requests C = 4 40.5 (49.9); 4 and 6 requests unchanged (C = 8 and 6).
+template <class DZ, class DT, bool kGrad, bool kShift>
+static int one_round_cluster_t(int vocab, int units) {
+  for (int c = kMaxCluster; c >= (kGrad ? 2 : 1); --c) {
+    const size_t smem = rowpass_smem<DZ, DT, kGrad>(rowpass_slice(vocab, c));
+    if (active_clusters<DZ, DT, kGrad, kShift>(c, smem) >= units) return c;
   }
   return 0;
 }
 
-template <bool kShift>
-static int one_round_cluster_dtypes(int z_dtype, int t_dtype, int vocab, int pairs) {
+template <bool kGrad, bool kShift>
+static int one_round_cluster_dtypes(int z_dtype, int t_dtype, int vocab, int units) {
   const bool zb = (z_dtype == 1), tb = (t_dtype == 1);
-  if (zb && tb) return one_round_cluster_t<BF16, BF16, kShift>(vocab, pairs);
-  if (!zb && tb) return one_round_cluster_t<F32, BF16, kShift>(vocab, pairs);
-  if (zb && !tb) return one_round_cluster_t<BF16, F32, kShift>(vocab, pairs);
-  return one_round_cluster_t<F32, F32, kShift>(vocab, pairs);
+  if (zb && tb) return one_round_cluster_t<BF16, BF16, kGrad, kShift>(vocab, units);
+  if (!zb && tb) return one_round_cluster_t<F32, BF16, kGrad, kShift>(vocab, units);
+  if (zb && !tb) return one_round_cluster_t<BF16, F32, kGrad, kShift>(vocab, units);
+  return one_round_cluster_t<F32, F32, kGrad, kShift>(vocab, units);
+}
+
+int rowpass_one_round_cluster(int z_dtype, int t_dtype, bool aligned, int vocab, int units) {
+  return aligned ? one_round_cluster_dtypes<false, false>(z_dtype, t_dtype, vocab, units)
+                 : one_round_cluster_dtypes<false, true>(z_dtype, t_dtype, vocab, units);
 }
 
 int rowpass_grad_one_round_cluster(int z_dtype, int t_dtype, bool aligned, int vocab, int pairs) {
-  return aligned ? one_round_cluster_dtypes<false>(z_dtype, t_dtype, vocab, pairs)
-                 : one_round_cluster_dtypes<true>(z_dtype, t_dtype, vocab, pairs);
+  return aligned ? one_round_cluster_dtypes<true, false>(z_dtype, t_dtype, vocab, pairs)
+                 : one_round_cluster_dtypes<true, true>(z_dtype, t_dtype, vocab, pairs);
 }
 
 int rowpass_grad_cluster_size(int vocab, int units, int row_bytes, int chunk_entries, int num_sms, long long l2_bytes) {
