@@ -335,11 +335,11 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
   p.grad = grad_draft;
   p.ld_g = ld_g;
   // The on-chip fused kernel holds whole row pairs in shared memory (rows on the
-  // 16-byte grid, at most one wave of row units); otherwise the row pass with the
-  // gradient, which reads the logits from HBM once and writes dz from a second pass
-  // over each slice served by L2 (any element-aligned rows): 219.8 us on a
-  // 128-request batch at V = 151936, against 277.9 us for the forward row pass and
-  // the backward kernel one after the other.
+  // 16-byte grid, a batch whose clusters all run at once with one CTA per SM);
+  // otherwise the row pass with the gradient, which reads the logits from HBM once and
+  // writes dz from a second pass over each slice served by L2 (any element-aligned
+  // rows): 219.8 us on a 128-request batch at V = 151936, against 277.9 us for the
+  // forward row pass and the backward kernel one after the other.
   const bool aligned16 = rows_16b(draft_logits, ld_d, dtype_bytes(d_dtype)) &&
                          rows_16b(target_logits, ld_t, dtype_bytes(t_dtype)) && rows_16b(grad_draft, ld_g, 4);
   const bool fused = aligned16 && num_draft_rows + num_requests <= fused_max_units(vocab, d_dtype, t_dtype, num_sms());

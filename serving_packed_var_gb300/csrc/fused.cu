@@ -20,6 +20,7 @@
 //   KL = sum_v min(term_v, c),  S = sum_v [term_v <= c] p_v (r_v + 1),
 //   dz_v = g ( p_v ([term_v <= c](r_v + 1) - S) + beta (p_v - [v == a]) ).
 // Target-only units (the bonus rows) only find their argmax.
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 #include <cmath>
@@ -38,10 +39,11 @@ constexpr uint32_t kPiece = 16384;  // bytes per bulk copy
 // The shared-memory budget: two resident CTAs per SM (a slice of a bf16 pair at
 // V = 151936 then needs clusters of 6).
 constexpr int kFCtasPerSm = 2;
-// The fused kernel takes batches of at most one wave of row units: beyond that its
-// phases, one after another inside each CTA, leave the HBM stream idle (a 128-request
-// batch at V = 151936: 384 us, against 219.8 us for the row pass with the gradient).
-constexpr int kFMaxWaves = 1;
+// The fused kernel takes batches whose clusters all run at once with one CTA per SM:
+// with two CTAs on an SM its phases, one after another inside each CTA, leave the HBM
+// stream idle, and the row pass with the gradient is faster (k = 16 per request at
+// V = 151936, bf16, graph-replayed: one request 16.4 us fused against 18.4; two
+// requests 22.5 fused against 20.5; a 128-request batch 384 us against 219.8).
 constexpr size_t kSmemPerSm = 227 * 1024;
 constexpr size_t kStaticReserve = 4096;  // static shared memory and the per-CTA reservation
 
@@ -493,7 +495,8 @@ template <class DZ, class DT>
 static int fused_max_units_t(int vocab, int num_sms) {
   const int C = fused_cluster_size(vocab, DZ::kBytes + DT::kBytes);
   if (C == 0) return 0;
-  return kFMaxWaves * fused_resident_clusters<DZ, DT>(C, fused_smem<DZ, DT>(rowpass_slice(vocab, C)), num_sms);
+  return std::min(fused_resident_clusters<DZ, DT>(C, fused_smem<DZ, DT>(rowpass_slice(vocab, C)), num_sms),
+                  num_sms / C);
 }
 
 template <class DZ, class DT>

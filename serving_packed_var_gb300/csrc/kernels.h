@@ -148,8 +148,9 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
 // dz on the 16-byte grid, the shift-free instance).
 cudaError_t launch_bwd(const BwdParams& p, int z_dtype, int t_dtype, bool aligned, cudaStream_t s);
 // Fused forward + backward (K4).  fused_max_units is the largest batch (draft rows +
-// requests) the fused kernel is used for: 0 when a row pair does not fit a cluster's
-// shared memory; above it the caller runs K1 + K3, which stream faster on full waves.
+// requests) the fused kernel is used for (its clusters all resident with one CTA per
+// SM): 0 when a row pair does not fit a cluster's shared memory; above it the caller
+// runs the row pass with the gradient, which streams faster.
 cudaError_t launch_fused(const RowPassParams& p, int z_dtype, int t_dtype, int num_sms, cudaStream_t s);
 int fused_cluster_size(int vocab, int bytes_per_entry);
 int fused_max_units(int vocab, int z_dtype, int t_dtype, int num_sms);

@@ -150,7 +150,7 @@ def test_edge_shapes(case):
     _close_to_separate(b, oracle_grad_rows=gsel)
 
 
-# More than one wave of row units: the single-pass row pass with the gradient (each
+# More row units than the on-chip kernel takes: the single-pass row pass with the gradient (each
 # slice read from HBM once; the second pass over it, for dz, is served by L2).
 STREAM = [
     dict(vocab=151936, k=[16] * 8),
@@ -170,7 +170,7 @@ def test_streaming_fwd_bwd_shapes(case):
 
 
 def test_streaming_per_row_weights():
-    # more row units than one wave of the on-chip kernel holds: the streaming pass with
+    # more row units than the on-chip kernel takes: the streaming pass with
     # an upstream weight per draft row
     w = custom(vocab=20000, k=[16, 7, 12, 3] * 12, clip_c=0.3)
     nd = w.num_draft_rows
