@@ -32,12 +32,12 @@ namespace {
 
 // S1: 256-thread CTAs with eight 16-byte loads in flight per thread, four resident
 // CTAs per SM; a row is split over a cluster of up to 8 CTAs while there are fewer
-// than 12 row units per SM.  S2: 256-thread CTAs, eight resident per SM, so that
-// 8 x 152 CTAs hold every request of a 128-request batch at once.
+// than 1.7 CTAs per SM (lse_cluster_size).  S2: 256-thread CTAs, eight resident per
+// SM, so that 8 x 152 CTAs hold every request of a 128-request batch at once.
 constexpr int kLseThreads = 256;
 constexpr int kLseUnroll = 8;  // 16-byte loads in flight per thread
 constexpr int kLseMinBlocks = 4;
-constexpr int kLseRowsPerSm = 12;
+constexpr int kLseCtasPerSmX10 = 17;  // 1.7 CTAs per SM
 constexpr int kDrawMinBlocks = 8;
 constexpr int kLseMaxCluster = 8;
 constexpr int kDrawThreads = 256;  // per CTA
@@ -553,12 +553,16 @@ __global__ void __launch_bounds__(kDrawThreads, kDrawMinBlocks) sampled_draw_ker
 // host side
 // ---------------------------------------------------------------------------
 
+// S1 splits each row over the fewest CTAs that give 1.7 CTAs per SM (at most 8).
+// Measured on GB300, k = 16 per request at V = 151936, bf16, us per sampled call (the
+// earlier rule, doubling C up to 12 rows per SM, in brackets): one request C = 8 14.4
+// graph-replayed (the same); 2 requests C = 4 16.4 (18.4); 4 requests C = 2 24.0
+// (26.5); 8 requests C = 1 27.6 eager (33.6); 16 requests C = 1 45.6 (48.7); 32
+// requests C = 1 67.9 (71.4).
 static int lse_cluster_size(int rows, int num_sms) {
-  int C = 1;
-  while (C < kLseMaxCluster &&
-         static_cast<int64_t>(rows) * C < static_cast<int64_t>(kLseRowsPerSm) * num_sms)
-    C *= 2;
-  return C;
+  const int64_t want = (static_cast<int64_t>(kLseCtasPerSmX10) * num_sms + 9) / 10;  // CTAs, rounded up
+  const int64_t c = (want + rows - 1) / rows;
+  return static_cast<int>(c < 1 ? 1 : (c > kLseMaxCluster ? kLseMaxCluster : c));
 }
 
 template <class DZ, class DT>
