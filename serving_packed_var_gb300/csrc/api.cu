@@ -4,6 +4,8 @@
 // return at once and enqueue nothing.  Every accepted call enqueues its kernels on
 // the caller's stream and returns without synchronising.
 #include <atomic>
+#include <mutex>
+#include <vector>
 #include <cmath>
 #include <cstdint>
 
@@ -47,40 +49,43 @@ bool int_ptr_ok(const void* p) { return p && aligned(p, 4); }
 
 // The device must be compute capability 10.3 (checked once per device).
 adaflash_status check_device() {
-  static int cache[64];  // 0 unknown, 1 ok, 2 unsupported
+  static std::atomic<int> cache[64];  // 0 unknown, 1 ok, 2 unsupported (host threads may race: same value)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ADAFLASH_ERR_CUDA;
-  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev] == 1 ? ADAFLASH_OK : ADAFLASH_ERR_UNSUPPORTED;
+  const int known = (dev >= 0 && dev < 64) ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (known) return known == 1 ? ADAFLASH_OK : ADAFLASH_ERR_UNSUPPORTED;
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return ADAFLASH_ERR_CUDA;
   const bool ok = (major == 10 && minor == 3);
-  if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+  if (dev >= 0 && dev < 64) cache[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
   return ok ? ADAFLASH_OK : ADAFLASH_ERR_UNSUPPORTED;
 }
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms() {
-  static int cache[64];
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  const int known = (dev >= 0 && dev < 64) ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (known) return known;
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 152;
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
 // L2 size of the current device in bytes (cached per device; 0 if unknown).
 long long l2_bytes() {
-  static long long cache[64];
+  static std::atomic<long long> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  const long long known = (dev >= 0 && dev < 64) ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (known) return known;
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n < 1) return 0;
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -111,6 +116,29 @@ adaflash_status empty_batch(float* loss, bool has_loss, const uint32_t* d_status
 namespace adaflash {
 static std::atomic<uint64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+cudaError_t raise_smem_limit(const void* fn, size_t bytes) {
+  struct Limit {
+    int device;
+    const void* fn;
+    size_t bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Limit> limits;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  Limit* found = nullptr;
+  for (Limit& l : limits)
+    if (l.device == device && l.fn == fn) found = &l;
+  if (found != nullptr && found->bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  if (found != nullptr) found->bytes = bytes;
+  else limits.push_back(Limit{device, fn, bytes});
+  return cudaSuccess;
+}
 }  // namespace adaflash
 
 extern "C" {

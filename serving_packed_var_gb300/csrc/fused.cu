@@ -24,6 +24,7 @@
 #include <cfloat>
 #include <climits>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -438,6 +439,7 @@ struct FOcc {
   int device;
   int clusters;
 };
+std::mutex g_focc_mu;
 FOcc g_focc[64];
 int g_focc_n = 0;
 }  // namespace
@@ -462,11 +464,14 @@ static int fused_resident_clusters(int C, size_t smem, int num_sms) {
   auto kern = fused_kernel<DZ, DT>;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return 0;
-  for (int i = 0; i < g_focc_n; ++i)
-    if (g_focc[i].fn == reinterpret_cast<const void*>(kern) && g_focc[i].cluster == C && g_focc[i].smem == smem &&
-        g_focc[i].device == device)
-      return g_focc[i].clusters;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess) {
+  {
+    std::lock_guard<std::mutex> lock(g_focc_mu);
+    for (int i = 0; i < g_focc_n; ++i)
+      if (g_focc[i].fn == reinterpret_cast<const void*>(kern) && g_focc[i].cluster == C && g_focc[i].smem == smem &&
+          g_focc[i].device == device)
+        return g_focc[i].clusters;
+  }
+  if (raise_smem_limit(reinterpret_cast<const void*>(kern), smem) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
@@ -487,6 +492,7 @@ static int fused_resident_clusters(int C, size_t smem, int num_sms) {
     clusters = num_sms / C;  // one CTA per SM: always resident
     if (clusters < 1) clusters = 1;
   }
+  std::lock_guard<std::mutex> lock(g_focc_mu);
   if (g_focc_n < 64) g_focc[g_focc_n++] = FOcc{reinterpret_cast<const void*>(kern), C, smem, device, clusters};
   return clusters;
 }
@@ -514,7 +520,7 @@ static cudaError_t launch_fused_t(const RowPassParams& p0, int num_sms, cudaStre
   auto kern = fused_kernel<DZ, DT>;
   const int clusters = fused_resident_clusters<DZ, DT>(C, smem, num_sms);
   if (clusters < 1) return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kFThreads, 1, 1);

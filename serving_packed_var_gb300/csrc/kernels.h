@@ -127,6 +127,10 @@ struct LmCombineParams {
 
 // Launch counter behind adaflash_kernel_launches (incremented once per launch).
 void count_launch();
+// Raises a kernel's dynamic shared-memory limit on the current device to at least
+// `bytes`, never lowering it, so host threads launching one kernel with different
+// sizes cannot undo each other's setting between setting it and launching.
+cudaError_t raise_smem_limit(const void* fn, size_t bytes);
 
 // dtype codes match adaflash_dtype (0 = fp32, 1 = bf16)
 // The row pass (rows at any element-aligned address: each row follows its target

@@ -746,11 +746,11 @@ cudaError_t launch_lm_gemm(const uint16_t* hd, int64_t ld_hd, const uint16_t* ht
                               : static_cast<size_t>(Ring<false>::kStages) * Ring<false>::kStage) +
                       4 * kBM * sizeof(EpiRec) + 1024;
   auto kern = shared ? lmhead_gemm_kernel<true> : lmhead_gemm_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 148;
+    sms = 152;
   const long long tiles = static_cast<long long>(m_tiles) * p.n_vtiles;
   const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);  // one CTA per SM (shared memory)
   count_launch();

@@ -44,9 +44,11 @@
 // label, per-vocabulary clipping) and the opening section (the target verifies the
 // draft; its argmax is the greedy choice).
 #include <algorithm>
+#include <atomic>
 #include <cfloat>
 #include <climits>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -777,18 +779,20 @@ struct OccEntry {
   int device;
   int clusters;
 };
-OccEntry g_occ[64];
+std::mutex g_occ_mu;
+OccEntry g_occ[256];
 int g_occ_n = 0;
 }  // namespace
 
 static int sm_count() {
-  static int cache[64];
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  const int known = (dev >= 0 && dev < 64) ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (known) return known;
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 152;
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -809,15 +813,18 @@ static int active_clusters(int cluster, size_t smem) {
   auto kern = rowpass_kernel<DZ, DT, kGrad, kShift>;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return 1;
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    for (int i = 0; i < g_occ_n; ++i)
+      if (g_occ[i].fn == reinterpret_cast<const void*>(kern) && g_occ[i].smem == smem &&
+          g_occ[i].cluster == cluster && g_occ[i].device == device)
+        return g_occ[i].clusters;
+  }
   // The query must see the shared-memory size the launch will use.
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess) {
+  if (raise_smem_limit(reinterpret_cast<const void*>(kern), smem) != cudaSuccess) {
     (void)cudaGetLastError();
     return 1;
   }
-  for (int i = 0; i < g_occ_n; ++i)
-    if (g_occ[i].fn == reinterpret_cast<const void*>(kern) && g_occ[i].smem == smem &&
-        g_occ[i].cluster == cluster && g_occ[i].device == device)
-      return g_occ[i].clusters;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
   cfg.blockDim = dim3(RowCfg<kGrad>::kThreads, 1, 1);
@@ -835,7 +842,8 @@ static int active_clusters(int cluster, size_t smem) {
     n = sm_count() / cluster;  // one CTA per SM: always resident
     if (n < 1) n = 1;
   }
-  if (g_occ_n < 64) g_occ[g_occ_n++] = OccEntry{reinterpret_cast<const void*>(kern), smem, cluster, device, n};
+  std::lock_guard<std::mutex> lock(g_occ_mu);
+  if (g_occ_n < 256) g_occ[g_occ_n++] = OccEntry{reinterpret_cast<const void*>(kern), smem, cluster, device, n};
   return n;
 }
 
@@ -846,7 +854,7 @@ static cudaError_t launch_range(const RowPassParams& p, bool programmatic, cudaS
   auto kern = rowpass_kernel<DZ, DT, kGrad, kShift>;
   const int units = p.unit_end - p.unit_begin;
   if (units <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const int clusters = active_clusters<DZ, DT, kGrad, kShift>(p.cluster, smem);
   cudaLaunchConfig_t cfg = {};
