@@ -150,6 +150,21 @@ __device__ __forceinline__ void grad_of8(const float z[8], const float t[8], con
   }
 }
 
+// Reuse of the ring by the second pass (with the gradient): when a slice has at least
+// kStages chunks, the last kStages chunks of the first pass are still in the ring, each
+// in the stage that the second pass's first kStages positions land in (position ci of
+// the second pass is ring position nch + ci after the first pass's 0 .. nch - 1).  They
+// come first, in ascending order, with no copy; the rest follow from L2, last chunk
+// first (the newest lines there).  With fewer chunks every chunk comes from L2.  The
+// first pass asks L2 to drop those last chunks at once rather than keep them.  Measured
+// on one box (us per call, 128 / 32 requests at V = 151936 bf16, ms on the 512-request
+// stress batch; every chunk from L2 in brackets): 217.4 (218.6), 79.4 (79.1), 2.441
+// (2.438); keeping the reused chunks in L2 as well: 219.6, 79.3, 2.465.
+__device__ __forceinline__ bool second_pass_reuses(int ci, int nch) { return nch >= kStages && ci < kStages; }
+__device__ __forceinline__ int second_pass_chunk(int ci, int nch) {
+  return second_pass_reuses(ci, nch) ? nch - kStages + ci : nch - 1 - ci;
+}
+
 // kGrad: the single-pass forward + backward for batches of many rows.  After a
 // pair unit's row constants and clip corrections are known, the producer's second
 // pass over the same slice (queued right behind the first, so it is served from L2:
@@ -264,14 +279,16 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
         const int nch = (body + kChunk - 1) / kChunk;
         for (int pass = 0; pass < passes && !*abort_flag; ++pass) {
           for (int ci = 0; ci < nch; ++ci, ++cc) {
-            // the second pass takes the slice last chunk first: those lines are the
-            // newest in L2
-            const int e0 = pass == 1 ? (nch - 1 - ci) * kChunk : ci * kChunk;
+            const int e0 = (pass == 1 ? second_pass_chunk(ci, nch) : ci) * kChunk;
             const int st = static_cast<int>(cc % kStages);
             if (cc >= static_cast<uint32_t>(kStages) &&
                 !mbar_wait_bounded(&empty_bar[st], ((cc / kStages) & 1) ^ 1)) {
               *abort_flag = 1;
               break;
+            }
+            if (pass == 1 && second_pass_reuses(ci, nch)) {
+              mbar_arrive(&full_bar[st]);  // the chunk is still in this stage
+              continue;
             }
             const int n = min(kChunk, body - e0);
             const uint32_t bz = U.pair ? static_cast<uint32_t>(n * DZ::kBytes + (zshift ? 16 : 0)) : 0u;
@@ -282,7 +299,9 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
             const uint8_t* tsrc = G.tb + static_cast<int64_t>(v_begin + e0) * DT::kBytes;
             if (kGrad && U.pair) {
               // L2 priority: keep the first pass's lines for the second, then drop them
-              const uint64_t pol = pass == 0 ? keep : drop;
+              // (and drop at once the chunks the second pass takes from the ring)
+              const bool reused = pass == 0 && nch >= kStages && ci >= nch - kStages;
+              const uint64_t pol = (pass == 0 && !reused) ? keep : drop;
               bulk_copy_g2s_hint(stage + kZOff, zsrc, bz, &full_bar[st], pol);
               bulk_copy_g2s_hint(stage, tsrc, bt, &full_bar[st], pol);
             } else {
@@ -652,7 +671,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
           dispatch_shift<DZ, kShift>(G.zs2, [&](auto zs_c) {
             constexpr int ZS = decltype(zs_c)::value;
             for (int ci = 0; ci < nch; ++ci, ++cc) {
-              const int e0 = (nch - 1 - ci) * kChunk;  // the producer's second-pass order
+              const int e0 = second_pass_chunk(ci, nch) * kChunk;  // the producer's second-pass order
               const int st = static_cast<int>(cc % kStages);
               if (!mbar_wait_bounded(&full_bar[st], (cc / kStages) & 1)) {
                 atomicOr(&s_unit_err, 1);
