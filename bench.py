@@ -803,15 +803,18 @@ def run_lmhead(args, w, dev, af, torch, np, stream):
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(n):
-        e2e_step()
-    torch.cuda.synchronize()
-    el = time.perf_counter() - t0
+    blocks = []
+    for _ in range(3):  # the median of three timed blocks, as for the step's end-to-end figure
+        t0 = time.perf_counter()
+        for _ in range(n):
+            e2e_step()
+        torch.cuda.synchronize()
+        blocks.append(time.perf_counter() - t0)
+    el = statistics.median(blocks)
     bi = sum(x.numel() * x.element_size() for x in (hdh, hth, tokh, doffh))
     bo = sum(x.numel() * x.element_size() for x in res_h.values())
     e2e = {"value": Nd * n / el, "unit": "rows/s", "ms_per_step": el / n * 1e3, "h2d_bytes_per_step": bi,
-           "d2h_bytes_per_step": bo, "steps": n,
+           "d2h_bytes_per_step": bo, "steps": n, "blocks_ms_per_step": [round(b / n * 1e3, 4) for b in blocks],
            "returns": "verification outputs and loss to host memory (the heads stay resident on the device)"}
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())} (lmhead e2e)")
@@ -884,15 +887,21 @@ def run_e2e(args, b, w, dev, af, torch, np, grad_to_host=False):
     for _ in range(3):
         step()
     torch.cuda.synchronize()
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        step()
-    torch.cuda.synchronize()
-    el = max_over_ranks(time.perf_counter() - t0, dev if int(os.environ.get("WORLD_SIZE", "1")) > 1 else None)
+    # three timed blocks, the median reported: a host-side stall in one block (the copies
+    # go through host memory) does not decide the figure
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    blocks = []
+    for _ in range(3):
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            step()
+        torch.cuda.synchronize()
+        blocks.append(max_over_ranks(time.perf_counter() - t0, dev if world > 1 else None))
+    el = statistics.median(blocks)
     return {"value": world * Nd * steps / el, "unit": "rows/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "steps": steps, "ms_per_step": el / steps * 1e3,
+            "blocks_ms_per_step": [round(b / steps * 1e3, 4) for b in blocks],
             "returns": ("verification outputs, loss and the float32 gradient to host memory" if grad_to_host else
                         "verification outputs and loss to host memory; the float32 gradient stays on the device "
                         "for an on-device optimiser step"),
