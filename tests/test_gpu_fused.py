@@ -154,6 +154,10 @@ def test_edge_shapes(case):
 # slice read from HBM once; the second pass over it, for dz, is served by L2).
 STREAM = [
     dict(vocab=151936, k=[16] * 8),
+    # paired rows that all fit the L2 at once: one round of clusters (C = 8, 8, 6 here)
+    dict(vocab=151936, k=[16] * 3),
+    dict(vocab=151936, k=[16] * 4, d_dtype="fp32", t_dtype="bf16"),
+    dict(vocab=151937, k=[16, 9, 16, 12, 16, 1], d_dtype="fp32", t_dtype="bf16"),
     dict(vocab=151936, k=[16, 3, 9, 1] * 6, d_dtype="fp32", t_dtype="bf16"),
     dict(vocab=40000, k=list(np.random.default_rng(11).integers(1, 17, size=200)), clip_c=0.05),
     dict(vocab=1000, k=[16] * 300, d_dtype="fp32", t_dtype="fp32"),

@@ -172,6 +172,15 @@ def test_constant_and_equal_rows():
     assert run.h["kl_row"][1] == 0.0 and run.h["kl_row"][4] == 0.0
 
 
+@pytest.mark.parametrize("requests", [3, 4, 6, 8, 16])
+def test_mid_batches_at_qwen3_vocab(requests):
+    # k = 16 per request at V = 151936: the forward and verification take every row in one round of
+    # resident clusters with the largest cluster size that allows it (8 down to 1 as the batch grows)
+    b = materialize(custom(vocab=151936, k=[16] * requests, d_dtype="bf16", t_dtype="bf16", seed=requests))
+    rng = np.random.default_rng(requests)
+    _full_check(b, grad_rows=sorted(set(rng.choice(b.w.num_draft_rows, 6, replace=False)) | {0, b.w.num_draft_rows - 1}))
+
+
 def test_many_requests_small_vocab():
     rng = np.random.default_rng(9)
     k = rng.integers(1, 17, size=700)
