@@ -9,23 +9,23 @@
 //   producer warp   : 1-D bulk copies (TMA engine) of chunks of z and t into a
 //                     ring of shared-memory stages (mbarrier-signalled), running
 //                     ahead across unit boundaries;
-//   8 consumer warps: per 8-entry group, an online log-sum-exp of z and of t,
-//                     sum_v e^{z_v}(z_v - t_v) (packed f32x2 arithmetic), a bound
-//                     on max_v (z_v - t_v), the lowest-index argmax of t, and the
-//                     largest group maximum of z each thread sees.
+//   consumer warps  : (8 in the forward, 4 with the gradient) per 8-entry group, an
+//                     online log-sum-exp of z and of t, sum_v e^{z_v}(z_v - t_v)
+//                     (packed f32x2 arithmetic), a bound on max_v (z_v - t_v), the
+//                     lowest-index argmax of t, and the largest group maximum of z
+//                     each thread sees.
 //
 // Slice results meet over distributed shared memory (asynchronous remote stores
 // that complete on the receiver's mbarrier, double-buffered by unit parity).  Every
-// CTA combines them in
-// the same fixed order and gets the row's log-sum-exps, the unclipped reverse KL
+// CTA combines them in the same fixed order and gets the row's log-sum-exps, the
+// unclipped reverse KL
 //     KL = sum_v p_v (z_v - t_v) - (lse_z - lse_t),
 // and the bound term_v = p_v r_v <= p_v R, R = max_v(z_v - t_v) - (lse_z - lse_t).
 // A term can exceed the clip c only where p_v > c / R, i.e. z_v > lse_z + log(c/R);
 // each thread compares the largest group maximum of z it saw with that threshold
 // (no exponentials) and only when it is above, its groups are re-read and the ones
-// above the threshold evaluated exactly.  The
-// clipped KL is KL - sum_{term_v > c} (term_v - c): each logit byte is read from
-// HBM once.
+// above the threshold evaluated exactly.  The clipped KL is
+// KL - sum_{term_v > c} (term_v - c): each logit byte is read from HBM once.
 //
 // Exponent offsets are integers in base 2 (n = -ceil(max * log2 e)), so every
 // rescale and every combine of partial sums multiplies by an exact power of two.
@@ -35,8 +35,8 @@
 // (n_t - n_z) ln 2 + ln(S_z / S_t), never as a difference of two large logs.
 //
 // The kGrad instantiation also writes dz: a second pass over each slice, served
-// from L2, once the row's constants and clip corrections are known (see the
-// comment at RowGrad below).
+// from the ring and from L2, once the row's constants and clip corrections are known
+// (see the comments at second_pass_chunk and RowGrad below).
 //
 // Operations: AdaFlash article ("AdaFlash: Adaptive Speculative Decoding with
 // Online Self-Improvement for High-Concurrency LLM Inference"), sections
