@@ -927,12 +927,16 @@ def run_reference(args):
     w = workload_from_args(args, make_workload, seed=0)
     b = materialize(w)
     base = None
+    # the whole run (warm-up and timed steps) is bounded to about two minutes of host time
+    # whatever K and W are: each step is a sample of at least one block of rows per thread
+    # count, with a time budget of 120 s / (K + W), at most 20 s
+    budget = max(0.02, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        cpu_baseline(b, budget_s=1.0)
+        cpu_baseline(b, budget_s=budget)
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        base = cpu_baseline(b, budget_s=max(1.0, min(20.0, 120.0 / max(1, args.steps))))
+        base = cpu_baseline(b, budget_s=budget)
         vals.append(base["value"])
     el = time.perf_counter() - t0
     value = statistics.mean(vals)
