@@ -111,6 +111,30 @@ adaflash_status empty_batch(float* loss, bool has_loss, const uint32_t* d_status
   return ADAFLASH_OK;
 }
 
+// The acceptance scan and loss kernel (K2) after a row pass: the verification outputs,
+// and the loss where kl_row is given.
+cudaError_t finalize_after(const int32_t* tokens, const int32_t* doff, const int32_t* target_argmax, int32_t R,
+                           int32_t N_d, int32_t V, int32_t* accept_len, int32_t* bonus_token, float* accept_rate,
+                           const float* kl_row, const float* ce_row, float ce_weight, float* loss, uint32_t* status,
+                           cudaStream_t s) {
+  FinalizeParams f = {};
+  f.tokens = tokens;
+  f.doff = doff;
+  f.target_argmax = target_argmax;
+  f.R = R;
+  f.N_d = N_d;
+  f.V = V;
+  f.accept_len = accept_len;
+  f.bonus_token = bonus_token;
+  f.accept_rate = accept_rate;
+  f.kl_row = kl_row;
+  f.ce_row = ce_row;
+  f.ce_weight = ce_weight;
+  f.loss = loss;
+  f.status = status;
+  return launch_finalize(f, s);
+}
+
 }  // namespace
 
 namespace adaflash {
@@ -192,18 +216,8 @@ adaflash_status adaflash_verify_packed(const void* target_logits, adaflash_dtype
   p.status = d_status;
   ADAFLASH_CUDA(launch_rowpass(p, 1, t_dtype, aligned, s));
 
-  FinalizeParams f = {};
-  f.tokens = draft_tokens;
-  f.doff = draft_offsets;
-  f.target_argmax = target_argmax;
-  f.R = num_requests;
-  f.N_d = num_draft_rows;
-  f.V = vocab;
-  f.accept_len = accept_len;
-  f.bonus_token = bonus_token;
-  f.accept_rate = accept_rate;
-  f.status = d_status;
-  ADAFLASH_CUDA(launch_finalize(f, s));
+  ADAFLASH_CUDA(finalize_after(draft_tokens, draft_offsets, target_argmax, num_requests, num_draft_rows, vocab,
+                               accept_len, bonus_token, accept_rate, nullptr, nullptr, 0.0f, nullptr, d_status, s));
   return ADAFLASH_OK;
 }
 
@@ -253,22 +267,8 @@ adaflash_status adaflash_opd_loss_fwd(const void* draft_logits, adaflash_dtype d
   p.status = d_status;
   ADAFLASH_CUDA(launch_rowpass(p, d_dtype, t_dtype, aligned, s));
 
-  FinalizeParams f = {};
-  f.tokens = draft_tokens;
-  f.doff = draft_offsets;
-  f.target_argmax = target_argmax;
-  f.R = num_requests;
-  f.N_d = num_draft_rows;
-  f.V = vocab;
-  f.accept_len = accept_len;
-  f.bonus_token = bonus_token;
-  f.accept_rate = accept_rate;
-  f.kl_row = kl_row;
-  f.ce_row = ce_row;
-  f.ce_weight = ce_weight;
-  f.loss = loss;
-  f.status = d_status;
-  ADAFLASH_CUDA(launch_finalize(f, s));
+  ADAFLASH_CUDA(finalize_after(draft_tokens, draft_offsets, target_argmax, num_requests, num_draft_rows, vocab,
+                               accept_len, bonus_token, accept_rate, kl_row, ce_row, ce_weight, loss, d_status, s));
   return ADAFLASH_OK;
 }
 
@@ -385,22 +385,8 @@ adaflash_status adaflash_opd_loss_fwd_bwd(const void* draft_logits, adaflash_dty
     ADAFLASH_CUDA(launch_rowpass_grad(p, d_dtype, t_dtype, aligned16, s));
   }
 
-  FinalizeParams f = {};
-  f.tokens = draft_tokens;
-  f.doff = draft_offsets;
-  f.target_argmax = target_argmax;
-  f.R = num_requests;
-  f.N_d = num_draft_rows;
-  f.V = vocab;
-  f.accept_len = accept_len;
-  f.bonus_token = bonus_token;
-  f.accept_rate = accept_rate;
-  f.kl_row = kl_row;
-  f.ce_row = ce_row;
-  f.ce_weight = ce_weight;
-  f.loss = loss;
-  f.status = d_status;
-  ADAFLASH_CUDA(launch_finalize(f, s));
+  ADAFLASH_CUDA(finalize_after(draft_tokens, draft_offsets, target_argmax, num_requests, num_draft_rows, vocab,
+                               accept_len, bonus_token, accept_rate, kl_row, ce_row, ce_weight, loss, d_status, s));
 
   return ADAFLASH_OK;
 }
@@ -548,22 +534,8 @@ adaflash_status adaflash_lmhead_opd_fwd(const void* draft_hidden, int64_t ld_hd,
   c.status = d_status;
   ADAFLASH_CUDA(launch_lm_combine(c, s));
 
-  FinalizeParams f = {};
-  f.tokens = draft_tokens;
-  f.doff = draft_offsets;
-  f.target_argmax = target_argmax;
-  f.R = num_requests;
-  f.N_d = num_draft_rows;
-  f.V = vocab;
-  f.accept_len = accept_len;
-  f.bonus_token = bonus_token;
-  f.accept_rate = accept_rate;
-  f.kl_row = kl_row;
-  f.ce_row = ce_row;
-  f.ce_weight = ce_weight;
-  f.loss = loss;
-  f.status = d_status;
-  ADAFLASH_CUDA(launch_finalize(f, s));
+  ADAFLASH_CUDA(finalize_after(draft_tokens, draft_offsets, target_argmax, num_requests, num_draft_rows, vocab,
+                               accept_len, bonus_token, accept_rate, kl_row, ce_row, ce_weight, loss, d_status, s));
   return ADAFLASH_OK;
 }
 
