@@ -34,7 +34,10 @@
  * DEVICE pointer owned by the caller.  They allocate nothing, keep no state between
  * calls and never synchronise: each call enqueues its kernels on `stream` (a
  * cudaStream_t; NULL is the legacy default stream) and returns.  Calls on one stream
- * run in order.  The packer entry points (below) work on host memory only.
+ * run in order.  Several host threads may call at once (each on its own stream): the
+ * small host-side tables the library fills on first use (occupancy per kernel and
+ * cluster size, kernel shared-memory limits, device attributes) are locked or atomic.
+ * The packer entry points (below) work on host memory only.
  *
  * Errors:
  *   - Argument errors found on the host are returned at once and nothing is
