@@ -31,8 +31,8 @@
  * output sets *loss = 0 (its loss pointer must be valid).
  *
  * Ownership and ordering: every pointer argument of the GPU entry points is a
- * DEVICE pointer owned by the caller.  They allocate nothing, keep no state between
- * calls and never synchronise: each call enqueues its kernels on `stream` (a
+ * DEVICE pointer owned by the caller.  They allocate no device memory, keep no device
+ * state between calls and never synchronise: each call enqueues its kernels on `stream` (a
  * cudaStream_t; NULL is the legacy default stream) and returns.  Calls on one stream
  * run in order.  Several host threads may call at once (each on its own stream): the
  * small host-side tables the library fills on first use (occupancy per kernel and
