@@ -71,7 +71,6 @@ constexpr int kFwdChunk = 8192;
 constexpr int kGradConsumerWarps = 4;
 constexpr int kGradMinBlocks = 4;
 constexpr int kGradChunk = 4096;
-constexpr int kStages = 3;
 
 template <bool kGrad>
 struct RowCfg {
@@ -99,6 +98,15 @@ struct StageLayout {
   static constexpr int kZOff = kChunk * DT::kBytes;
   static constexpr int kBytes = (kZOff + kChunk * DZ::kBytes + 16 + 127) / 128 * 128;
 };
+
+// Ring stages: three; four in the pass with the gradient when one input is float32 and
+// the other bf16, whose 2048-entry stages are a quarter smaller than the bf16 pair's, so
+// that the ring keeps about the same bytes (and the second pass takes four chunks from
+// it instead of three).
+template <class DZ, class DT, bool kGrad>
+__host__ __device__ constexpr int stages_of() {
+  return (kGrad && DZ::kBytes + DT::kBytes == 6) ? 4 : 3;
+}
 
 
 }  // namespace
@@ -160,9 +168,13 @@ __device__ __forceinline__ void grad_of8(const float z[8], const float t[8], con
 // on one box (us per call, 128 / 32 requests at V = 151936 bf16, ms on the 512-request
 // stress batch; every chunk from L2 in brackets): 217.4 (218.6), 79.4 (79.1), 2.441
 // (2.438); keeping the reused chunks in L2 as well: 219.6, 79.3, 2.465.
-__device__ __forceinline__ bool second_pass_reuses(int ci, int nch) { return nch >= kStages && ci < kStages; }
+template <int kStages>
+__device__ __forceinline__ bool second_pass_reuses(int ci, int nch) {
+  return nch >= kStages && ci < kStages;
+}
+template <int kStages>
 __device__ __forceinline__ int second_pass_chunk(int ci, int nch) {
-  return second_pass_reuses(ci, nch) ? nch - kStages + ci : nch - 1 - ci;
+  return second_pass_reuses<kStages>(ci, nch) ? nch - kStages + ci : nch - 1 - ci;
 }
 
 // kGrad: the single-pass forward + backward for batches of many rows.  After a
@@ -188,6 +200,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
     rowpass_kernel(const RowPassParams P) {
   constexpr int kConsumerWarps = RowCfg<kGrad>::kWarps;
   constexpr int kConsumers = RowCfg<kGrad>::kConsumers;
+  constexpr int kStages = stages_of<DZ, DT, kGrad>();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages];
   __shared__ uint64_t empty_bar[kStages];
@@ -279,14 +292,14 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
         const int nch = (body + kChunk - 1) / kChunk;
         for (int pass = 0; pass < passes && !*abort_flag; ++pass) {
           for (int ci = 0; ci < nch; ++ci, ++cc) {
-            const int e0 = (pass == 1 ? second_pass_chunk(ci, nch) : ci) * kChunk;
+            const int e0 = (pass == 1 ? second_pass_chunk<kStages>(ci, nch) : ci) * kChunk;
             const int st = static_cast<int>(cc % kStages);
             if (cc >= static_cast<uint32_t>(kStages) &&
                 !mbar_wait_bounded(&empty_bar[st], ((cc / kStages) & 1) ^ 1)) {
               *abort_flag = 1;
               break;
             }
-            if (pass == 1 && second_pass_reuses(ci, nch)) {
+            if (pass == 1 && second_pass_reuses<kStages>(ci, nch)) {
               mbar_arrive(&full_bar[st]);  // the chunk is still in this stage
               continue;
             }
@@ -671,7 +684,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
           dispatch_shift<DZ, kShift>(G.zs2, [&](auto zs_c) {
             constexpr int ZS = decltype(zs_c)::value;
             for (int ci = 0; ci < nch; ++ci, ++cc) {
-              const int e0 = second_pass_chunk(ci, nch) * kChunk;  // the producer's second-pass order
+              const int e0 = second_pass_chunk<kStages>(ci, nch) * kChunk;  // the producer's second-pass order
               const int st = static_cast<int>(cc % kStages);
               if (!mbar_wait_bounded(&full_bar[st], (cc / kStages) & 1)) {
                 atomicOr(&s_unit_err, 1);
@@ -819,7 +832,7 @@ template <class DZ, class DT, bool kGrad>
 static size_t rowpass_smem(int slice) {
   constexpr int kChunk = chunk_of<DZ, DT, kGrad>();
   constexpr int kConsumers = RowCfg<kGrad>::kConsumers;
-  const size_t ring = static_cast<size_t>(kStages) * StageLayout<DZ, DT, kGrad>::kBytes;
+  const size_t ring = static_cast<size_t>(stages_of<DZ, DT, kGrad>()) * StageLayout<DZ, DT, kGrad>::kBytes;
   // screening codes: per consumer thread one slot per ring chunk, +1 for its one
   // directly loaded group (the ragged end of the slice or the head)
   const int slots = (slice + kChunk - 1) / kChunk + 1;

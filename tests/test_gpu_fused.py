@@ -162,6 +162,11 @@ STREAM = [
     dict(vocab=40000, k=list(np.random.default_rng(11).integers(1, 17, size=200)), clip_c=0.05),
     dict(vocab=1000, k=[16] * 300, d_dtype="fp32", t_dtype="fp32"),
     dict(vocab=151936, k=[16, 5, 11] * 4, d_dtype="fp32", t_dtype="fp32", clip_c=0.2),
+    # one float32 input and one bf16: a four-stage ring, so slices of three to six chunks take
+    # the second pass's first chunks from the ring and the rest from memory
+    dict(vocab=24577, k=[16] * 40, d_dtype="fp32", t_dtype="bf16"),
+    dict(vocab=12291, k=[16, 7] * 30, d_dtype="bf16", t_dtype="fp32"),
+    dict(vocab=49153, k=[16, 2] * 24, d_dtype="fp32", t_dtype="bf16"),
 ]
 
 
