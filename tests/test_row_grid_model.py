@@ -81,3 +81,63 @@ def test_large_rows(V):
             for off in offs:
                 for chunk, consumers in SHAPES[:2]:
                     visit_row(V, C, off, elem_bytes, chunk, consumers)
+
+
+# ---------------------------------------------------------------------------------------------
+# The second pass's reuse of the ring (the row pass with the gradient).
+#
+# Ring position cc (counted over the CTA's whole life) uses stage cc mod S.  A paired row queues
+# its nch chunks twice: the first pass in order, then the second pass, whose first min(S, nch)
+# positions take, when nch >= S, the first pass's last S chunks in ascending order without a copy
+# (the stage still holds them), and whose other positions copy the remaining chunks last one
+# first.  The first pass asks L2 to drop at once exactly the chunks the second pass takes from the
+# ring.  The model replays that order over a sequence of units and checks that each reused stage
+# still holds the chunk the second pass wants, that the second pass sees every chunk once, and that
+# the early-drop set is the reused set.  A slip such as reusing when nch < S, or an off-by-one in
+# the chunk a reused position maps to, fails it.
+
+
+def second_pass_reuses(ci, nch, S):
+    return nch >= S and ci < S
+
+
+def second_pass_chunk(ci, nch, S):
+    return nch - S + ci if second_pass_reuses(ci, nch, S) else nch - 1 - ci
+
+
+def replay_ring(units, S):
+    stage = [None] * S  # (unit, chunk) each stage holds
+    cc = 0
+    for u, (nch, passes) in enumerate(units):
+        dropped_early = set()
+        for ci in range(nch):  # first pass
+            stage[cc % S] = (u, ci)
+            if passes == 2 and nch >= S and ci >= nch - S:
+                dropped_early.add(ci)
+            cc += 1
+        if passes == 1:
+            continue
+        seen, reused = [], set()
+        for ci in range(nch):  # second pass
+            want = second_pass_chunk(ci, nch, S)
+            if second_pass_reuses(ci, nch, S):
+                assert stage[cc % S] == (u, want), ("stage no longer holds the chunk", u, nch, S, ci)
+                reused.add(want)
+            else:
+                stage[cc % S] = (u, want)
+            seen.append(want)
+            cc += 1
+        assert sorted(seen) == list(range(nch)), ("second pass order", nch, S)
+        assert reused == dropped_early, ("early drop set", nch, S)
+        if nch >= S:  # the reused chunks come first, ascending
+            assert seen[:S] == list(range(nch - S, nch))
+
+
+@pytest.mark.parametrize("S", [3, 4])
+def test_second_pass_reuse_of_the_ring(S):
+    for nch in range(0, 14):
+        replay_ring([(nch, 2)], S)
+    import random
+    rng = random.Random(5 + S)
+    for _ in range(200):  # paired rows (two passes) and bonus rows (one) in any order
+        replay_ring([(rng.randrange(0, 14), rng.choice((1, 2))) for _ in range(rng.randrange(1, 9))], S)
