@@ -224,6 +224,14 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
   const int cid = static_cast<int>(blockIdx.x) / C;
   const int ncl = static_cast<int>(gridDim.x) / C;
   const int num_units = P.unit_end;
+  // Unit order.  Units are paired rows, then target-only rows; cluster cid takes every
+  // ncl-th unit from cid on.  With the gradient, when one launch takes every unit, a
+  // quarter of a wave of target-only rows (one cheap pass each) moves to the front, so
+  // that a quarter of the clusters start their paired rows one short row later and the
+  // clusters' first passes, exchanges and dz writes do not all fall in step; the other
+  // target-only rows stay last, where they fill the final partial wave.
+  const int early = (kGrad && P.unit_begin == 0 && P.unit_end == P.N_d + P.R) ? min(P.R, ncl / 4) : 0;
+  auto unit_at = [&](int u) { return u < early ? P.N_d + u : (u < P.N_d + early ? u - early : u); };
 
   constexpr int kChunk = chunk_of<DZ, DT, kGrad>();
   constexpr int kGroupsPerThread = kChunk / 8 / kConsumers;  // 8-entry groups per consumer thread per chunk
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
         drop = l2_policy_evict_first();
       }
       for (int u = P.unit_begin + cid; u < num_units && !*abort_flag; u += ncl) {
-        const Unit U = map_unit(P, u);
+        const Unit U = map_unit(P, unit_at(u));
         const uint8_t* zrow =
             U.pair ? static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(U.d) * P.ld_z * DZ::kBytes : nullptr;
         const uint8_t* trow =
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(RowCfg<kGrad>::kThreads, RowCfg<kGrad>::kMinBl
     uint32_t cc = 0;
     int it = 0, pit = 0;
     for (int u = P.unit_begin + cid; u < num_units; u += ncl, ++it) {
-      const Unit U = map_unit(P, u);
+      const Unit U = map_unit(P, unit_at(u));
       const uint8_t* zrow =
           U.pair ? static_cast<const uint8_t*>(P.z) + static_cast<int64_t>(U.d) * P.ld_z * DZ::kBytes : nullptr;
       const uint8_t* trow =
