@@ -141,3 +141,32 @@ def test_second_pass_reuse_of_the_ring(S):
     rng = random.Random(5 + S)
     for _ in range(200):  # paired rows (two passes) and bonus rows (one) in any order
         replay_ring([(rng.randrange(0, 14), rng.choice((1, 2))) for _ in range(rng.randrange(1, 9))], S)
+
+
+# ---------------------------------------------------------------------------------------------
+# Unit order of the row pass with the gradient.  Units 0 .. N_d - 1 are the paired rows and
+# N_d .. N_d + R - 1 the target-only rows; cluster cid takes positions cid, cid + ncl, ...  When
+# one launch takes every unit, the first `early` = min(R, ncl // 4) positions hold target-only
+# rows, then come all paired rows, then the remaining target-only rows.  The model checks that
+# the order is a permutation (every row handled once), that exactly `early` clusters start with
+# a target-only row, and that the paired rows keep their relative order.
+
+
+def unit_at(u, N_d, R, ncl, whole_launch=True):
+    early = min(R, ncl // 4) if whole_launch else 0
+    return N_d + u if u < early else (u - early if u < N_d + early else u)
+
+
+@pytest.mark.parametrize("N_d,R,ncl", [(914, 128, 97), (289, 32, 101), (8192, 512, 97), (16, 1, 152),
+                                       (3, 3, 4), (0, 5, 8), (40, 0, 20), (5, 200, 64)])
+def test_unit_order_is_a_permutation(N_d, R, ncl):
+    n = N_d + R
+    order = [unit_at(u, N_d, R, ncl) for u in range(n)]
+    assert sorted(order) == list(range(n))
+    early = min(R, ncl // 4)
+    starts_target_only = sum(1 for cid in range(min(ncl, n)) if order[cid] >= N_d)
+    # the early rows, plus first positions that lie past every paired row (tiny batches)
+    assert starts_target_only == early + max(0, min(ncl, n) - (N_d + early))
+    paired = [x for x in order if x < N_d]
+    assert paired == list(range(N_d))
+    assert [unit_at(u, N_d, R, ncl, whole_launch=False) for u in range(n)] == list(range(n))
